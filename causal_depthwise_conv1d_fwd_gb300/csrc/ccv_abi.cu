@@ -1,0 +1,22 @@
+// Status strings and version of the ccv C ABI.
+#include "ccv_common.cuh"
+
+extern "C" const char *ccv_status_string(int status) {
+    switch (status) {
+        case CCV_OK: return "ok";
+        case CCV_ERR_NULL_POINTER: return "a required pointer is NULL";
+        case CCV_ERR_WIDTH: return "width must be in 2..5";
+        case CCV_ERR_SIZE: return "a size is negative, inconsistent or too large";
+        case CCV_ERR_STATE_LEN: return "conv_state has fewer columns than the method needs";
+        case CCV_ERR_ALIAS: return "an output overlaps an input it may not alias";
+        case CCV_ERR_STRIDE: return "a stride is negative";
+        case CCV_ERR_RANGE: return "the stream slice [off_s, off_s+ws) leaves the cache's D range";
+        case CCV_ERR_CAPACITY: return "an output buffer is smaller than the padded token count";
+        case CCV_ERR_ARGUMENT: return "has_initial_state needs conv_states";
+        default: break;
+    }
+    if (status > 0) return cudaGetErrorString(static_cast<cudaError_t>(status));
+    return "unknown ccv status";
+}
+
+extern "C" int ccv_version(void) { return 1 * 10000 + 0 * 100 + 0; }

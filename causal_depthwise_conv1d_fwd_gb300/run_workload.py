@@ -1,0 +1,71 @@
+"""Run one entry point on one of the named benchmark workloads a few times.
+
+Used to give a profiler a small, self-contained program:
+
+    python -m causal_depthwise_conv1d_fwd_gb300.run_workload --part prefill_tokens_dim --reps 3
+
+Parts: prefill_tokens_dim, prefill_dim_tokens (4 x 4096 tokens, dim 8192),
+decode (256 x 8192), paged (H16 x ws128, 32 requests; metadata + conv).
+The process exits 0 after a device synchronize; it times nothing.
+"""
+from __future__ import annotations
+
+import argparse
+
+import torch
+
+from . import api
+from . import workloads as wl
+
+PARTS = ("prefill_tokens_dim", "prefill_dim_tokens", "decode", "paged")
+
+
+def _dev(kwargs, dev):
+    return {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in kwargs.items()}
+
+
+def make_launch(part: str, dev):
+    if part.startswith("prefill"):
+        layout = "tokens_dim" if part.endswith("tokens_dim") else "dim_tokens"
+        d = _dev(wl.config_large_prefill(layout=layout).kwargs(), dev)
+        out = torch.empty_strided(d["x"].shape, d["x"].stride(), dtype=torch.bfloat16,
+                                  device=dev)
+        launch = api.prepare_ccv_fwd(**d, out=out)
+        return lambda: launch()
+    if part == "decode":
+        launch = api.prepare_ccv_update(**_dev(wl.config_decode().kwargs(), dev))
+        return lambda: launch()
+    if part == "paged":
+        c = wl.config_paged()
+        d = _dev(c.kwargs(), dev)
+        seq = torch.empty(c.T, dtype=torch.int32, device=dev)
+        qs = torch.empty(c.T, dtype=torch.int32, device=dev)
+        d["seq_idx"], d["query_start"] = seq, qs
+        meta = api.prepare_paged_sconv_seq_metadata(c.query_start_loc.to(dev),
+                                                    len(c.req_lengths), c.num_actual_tokens,
+                                                    seq, qs, c.T)
+        conv = api.prepare_paged_sconv_fwd(**d)
+
+        def run():
+            meta()
+            conv()
+        return run
+    raise ValueError(f"unknown part {part!r}; choose from {PARTS}")
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--part", choices=PARTS, required=True)
+    ap.add_argument("--reps", type=int, default=3)
+    args = ap.parse_args(argv)
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    run = make_launch(args.part, dev)
+    for _ in range(args.reps):
+        run()
+    torch.cuda.synchronize()
+    print(f"run_workload: {args.part} x{args.reps} ok")
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,169 @@
+"""The C ABI library on a host without a GPU: it builds, loads, exports every
+function include/ccv.h declares, and rejects bad arguments with the documented
+status codes before touching the device.  Fake (never dereferenced) pointer
+values are used; a call that passes validation would try to launch, so every
+call here is built to fail validation or to be empty work.
+"""
+from __future__ import annotations
+
+import ctypes
+import re
+import subprocess
+
+import pytest
+import torch
+
+from causal_depthwise_conv1d_fwd_gb300 import _lib, build
+
+OK, NULLP, WIDTH, SIZE, STATE, ALIAS, STRIDE, RANGE, CAP, ARG = 0, -1, -2, -3, -4, -5, -6, -7, -8, -9
+A, B, C = 0x10000, 0x2000000, 0x8000000  # fake 16-byte-aligned device addresses, far apart
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def test_every_declared_function_is_exported(lib):
+    names = _lib.declared_functions()
+    assert set(names) == {"ccv_status_string", "ccv_version", "ccv_fwd", "ccv_update",
+                          "paged_sconv_seq_metadata", "paged_sconv_fwd"}
+    out = subprocess.run(["nm", "-D", "--defined-only", build.LIB], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r" T (\w+)$", out, flags=re.M))
+    for n in names:
+        assert n in exported, n
+        assert getattr(lib, n) is not None
+    assert set(names) == set(_lib.SIGNATURES)
+
+
+def test_status_strings(lib):
+    for code in (OK, NULLP, WIDTH, SIZE, STATE, ALIAS, STRIDE, RANGE, CAP, ARG):
+        s = _lib.status_string(code)
+        assert s and "unknown" not in s
+    assert "unknown" in _lib.status_string(-1000)
+    assert lib.ccv_version() == 10000
+
+
+def fwd(lib, **over):
+    args = dict(x=A, xsd=1, xst=64, out=B, osd=1, ost=64, w=C, wsd=4, wsw=1, bias=None,
+                st=C + 4096, ssl=192, ssd=1, sst=64, nl=4, sl=3, qsl=C + 8192, batch=2,
+                ci=None, hi=None, dim=64, total=10, width=4, pad=-1, silu=1, err=None,
+                stream=None)
+    args.update(over)
+    return lib.ccv_fwd(*args.values())
+
+
+def test_fwd_validation(lib):
+    assert fwd(lib, width=1) == WIDTH
+    assert fwd(lib, width=6) == WIDTH
+    assert fwd(lib, dim=-1) == SIZE
+    assert fwd(lib, batch=-2) == SIZE
+    assert fwd(lib, xst=-64) == STRIDE
+    assert fwd(lib, sst=-1) == STRIDE
+    assert fwd(lib, sl=2) == STATE
+    assert fwd(lib, st=None, hi=C + 12288) == ARG
+    assert fwd(lib, x=None) == NULLP
+    assert fwd(lib, qsl=None) == NULLP
+    assert fwd(lib, out=A + 64) == ALIAS  # overlaps x
+    # empty work succeeds without launching anything
+    assert fwd(lib, total=0) == OK
+    assert fwd(lib, batch=0) == OK
+    assert fwd(lib, dim=0) == OK
+    assert fwd(lib, total=0, x=None, out=None) == OK
+
+
+def test_fwd_valid_call_reports_cuda_error_without_gpu(lib):
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; this checks the no-device error path")
+    status = fwd(lib)
+    assert status > 0  # a cudaError_t from the failed launch
+    assert _lib.status_string(status)
+
+
+def upd(lib, **over):
+    args = dict(x=A, xsb=64, xsd=1, xst=1, out=A, osb=64, osd=1, ost=1, w=C, wsd=4, wsw=1,
+                bias=None, st=B, ssl=192, ssd=1, sst=64, nl=8, sl=3, idx=None, batch=4, dim=64,
+                seqlen=1, width=4, pad=-1, silu=1, err=None, stream=None)
+    args.update(over)
+    return lib.ccv_update(*args.values())
+
+
+def test_update_validation(lib):
+    assert upd(lib, width=7) == WIDTH
+    assert upd(lib, seqlen=-1) == SIZE
+    assert upd(lib, ssd=-1) == STRIDE
+    assert upd(lib, seqlen=2, sl=3) == STATE  # needs W-2+seqlen = 4 columns
+    assert upd(lib, sl=2) == STATE
+    assert upd(lib, st=None) == NULLP
+    assert upd(lib, out=A + 2) == ALIAS  # overlapping but not identical to x
+    assert upd(lib, batch=0) == OK
+    assert upd(lib, seqlen=0) == OK
+
+
+def meta(lib, **over):
+    args = dict(qsl=A, n_req=3, n_act=10, n_pad=16, seq=B, qs=C, cap=16, stream=None)
+    args.update(over)
+    return lib.paged_sconv_seq_metadata(*args.values())
+
+
+def test_metadata_validation(lib):
+    assert meta(lib, n_pad=9) == SIZE
+    assert meta(lib, cap=15) == CAP
+    assert meta(lib, n_req=0) == SIZE
+    assert meta(lib, seq=None) == NULLP
+    assert meta(lib, n_act=0, n_pad=0) == OK
+    assert meta(lib, n_req=-1) == SIZE
+
+
+def paged(lib, **over):
+    args = dict(x=A, xst=2048, cache=B, csb=16 * 16 * 512, csh=16 * 512, csn=512, nb=1024, H=16,
+                N=16, D=512, w=C, wsc=4, wsw=1, out=C + 65536, ost=2048, pos=C + 2 * 65536,
+                sidx=C + 3 * 65536, slot=C + 4 * 65536, bt=C + 5 * 65536, btr=200, btrows=32,
+                maxb=200, qs=C + 6 * 65536, T=8, off_s=128, ws=128, width=4, silu=1, resid=1,
+                err=None, stream=None)
+    args.update(over)
+    return lib.paged_sconv_fwd(*args.values())
+
+
+def test_paged_validation(lib):
+    assert paged(lib, width=9) == WIDTH
+    assert paged(lib, off_s=400) == RANGE  # 400 + 128 > 512
+    assert paged(lib, off_s=-8) == RANGE
+    assert paged(lib, H=0) == SIZE
+    assert paged(lib, maxb=0) == SIZE
+    assert paged(lib, csn=-512) == STRIDE
+    assert paged(lib, bt=None) == NULLP
+    assert paged(lib, out=A + 16) == ALIAS
+    assert paged(lib, T=0) == OK
+
+
+def test_binding_rejects_cpu_tensors():
+    import causal_depthwise_conv1d_fwd_gb300 as ccv
+    from causal_depthwise_conv1d_fwd_gb300 import workloads as wl
+
+    case = wl.varlen_prefill(1, [3, 2], 16, 4)
+    with pytest.raises(TypeError):
+        ccv.ccv_fwd(**case.kwargs())
+    d = wl.decode(2, 2, 16, 4)
+    with pytest.raises(TypeError):
+        ccv.ccv_update(**d.kwargs())
+    p = wl.paged(3, [2], [0], H=1, ws=8, N=4, D=8, num_blocks=4, off_s=0)
+    with pytest.raises(TypeError):
+        ccv.paged_sconv_fwd(**p.kwargs())
+
+
+def test_product_path_does_not_touch_the_oracle():
+    """The package must never import the oracle (no CPU fallback)."""
+    import os
+
+    from causal_depthwise_conv1d_fwd_gb300 import build as b
+
+    pkg = os.path.dirname(b.__file__)
+    for root, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(root, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "ccv_oracle" not in text, f

@@ -1,0 +1,254 @@
+"""GPU parity of ccv_fwd (varlen prefill) against the CPU oracle.
+
+Outputs within 1e-2*|ref| + 2e-5, conv_state bit-exact, untouched regions
+(pad sequences, zero-length sequences, wider state columns, guard bands)
+bit-exact.  Sizes span several chunks and ragged tails of both kernels
+(channel-last chunks of 128 tokens; channel-first chunks of 2048 tokens for
+aligned rows and 256 for the strided fallback).
+"""
+from __future__ import annotations
+
+import pytest
+import torch
+
+import oracle
+import causal_depthwise_conv1d_fwd_gb300 as ccv
+from causal_depthwise_conv1d_fwd_gb300 import workloads as wl
+from parity_util import assert_bits, assert_close, sentinel_like, to_device
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda", 0)
+
+
+def run_both(case, out_cpu=None, out_dev=None, err=False):
+    """Run the oracle and the GPU on the same inputs; return both results."""
+    ref_states = None if case.conv_states is None else case.conv_states.clone()
+    ref_out = sentinel_like(case.x) if out_cpu is None else out_cpu
+    oracle.ccv_fwd(case.x, case.weight, case.bias, ref_states, case.query_start_loc,
+                   case.cache_indices, case.has_initial_state, case.activation,
+                   case.pad_slot_id, out=ref_out)
+    d = to_device(case.kwargs(), DEV)
+    out = sentinel_like(d["x"]) if out_dev is None else out_dev
+    err_t = torch.zeros(1, dtype=torch.int32, device=DEV) if err else None
+    ccv.ccv_fwd(**d, out=out, err_count=err_t)
+    torch.cuda.synchronize()
+    return ref_out, ref_states, out, d["conv_states"], err_t
+
+
+def check(case, **kw):
+    ref_out, ref_states, out, states, _ = run_both(case, **kw)
+    assert_close(out, ref_out, f"{case.name} out")
+    assert_bits(out.isnan(), ref_out.isnan(), f"{case.name} nan pattern")
+    if ref_states is not None:
+        assert_bits(states, ref_states, f"{case.name} conv_states")
+
+
+# ------------------------------------------------------------ the configs ----
+
+def test_config_single_sequence():
+    check(wl.config_single())
+
+
+@pytest.mark.parametrize("layout", ["tokens_dim", "dim_tokens"])
+def test_config_varlen_batch(layout):
+    check(wl.config_varlen(layout=layout))
+
+
+@pytest.mark.parametrize("layout", ["tokens_dim", "dim_tokens"])
+def test_config_large_prefill_full_size(layout):
+    """4 x 4096 tokens, dim 8192: every output element, as the bench launches it."""
+    check(wl.config_large_prefill(layout=layout))
+
+
+# ------------------------------------------------------------- edge cases ----
+
+LENGTHS = [1, 2, 3, 4, 5, 127, 128, 129, 255, 0, 300, 31, 33]
+
+
+@pytest.mark.parametrize("width", [2, 3, 4, 5])
+@pytest.mark.parametrize("layout", ["tokens_dim", "dim_tokens"])
+def test_widths_and_ragged_chunks(width, layout):
+    case = wl.varlen_prefill(200 + width, LENGTHS, 40, width, num_cache_lines=20,
+                             layout=layout, pad_positions=(4,), has_init="bernoulli")
+    check(case)
+
+
+@pytest.mark.parametrize("layout", ["tokens_dim", "dim_tokens"])
+def test_long_sequences_span_many_chunks(layout):
+    case = wl.varlen_prefill(301, [2500, 7, 4100, 1], 24, 4, num_cache_lines=4,
+                             layout=layout, has_init="all")
+    check(case)
+
+
+@pytest.mark.parametrize("dim", [1, 7, 100, 264])
+@pytest.mark.parametrize("layout", ["tokens_dim", "dim_tokens"])
+def test_dims_not_multiple_of_eight(dim, layout):
+    case = wl.varlen_prefill(400 + dim, [9, 130, 1, 45], dim, 4, num_cache_lines=5,
+                             layout=layout, has_init="bernoulli")
+    check(case)
+
+
+@pytest.mark.parametrize("extra", [0, 1, 3, 5])
+def test_channel_first_unaligned_rows(extra):
+    """Channel-first x whose row length is not a multiple of 8 tokens: rows
+    start at different 16-byte phases (and tokens past the last sequence are
+    not processed)."""
+    case = wl.varlen_prefill(500 + extra, [13, 2049, 6, 300], 16, 4, num_cache_lines=4,
+                             layout="dim_tokens", has_init="all", extra_tokens=extra)
+    check(case)
+
+
+def test_mixed_layouts_use_generic_path():
+    case = wl.varlen_prefill(601, [17, 140, 3], 24, 4, num_cache_lines=3, layout="tokens_dim",
+                             has_init="bernoulli")
+    out_cpu = sentinel_like(case.x.t().contiguous().t().contiguous())  # (dim, T) channel-first
+    out_dev = sentinel_like(out_cpu, DEV)
+    ref_out, ref_states, out, states, _ = run_both(case, out_cpu=out_cpu, out_dev=out_dev)
+    assert_close(out, ref_out, "mixed out")
+    assert_bits(states, ref_states, "mixed states")
+
+
+def test_strided_views():
+    """x and out as every third row of wider buffers: stride over channels 1,
+    stride over tokens 90 (not a multiple of 8), so the strided kernel runs."""
+    base = wl.varlen_prefill(701, [11, 50, 4], 30, 4, num_cache_lines=3, layout="tokens_dim",
+                             has_init="all")
+    T = base.total_tokens
+
+    def spread(t_dim_major, device):
+        wide = torch.zeros(T * 3, 30, dtype=torch.bfloat16, device=device)
+        wide.view(torch.int16).fill_(-99)
+        wide[::3] = t_dim_major.t().to(device)
+        return wide, wide[::3].t()
+
+    _, x_cpu = spread(base.x, "cpu")
+    wide_out_cpu, out_cpu = spread(base.x, "cpu")
+    out_cpu.view(torch.int16).fill_(-12345)
+    ref_states = base.conv_states.clone()
+    oracle.ccv_fwd(x_cpu, base.weight, base.bias, ref_states, base.query_start_loc,
+                   base.cache_indices, base.has_initial_state, base.activation, -1, out=out_cpu)
+    d = to_device(base.kwargs(), DEV)
+    _, d["x"] = spread(base.x, DEV)
+    wide_out, out = spread(base.x, DEV)
+    out.view(torch.int16).fill_(-12345)
+    assert d["x"].stride() == (1, 90) and out.stride() == (1, 90)
+    ccv.ccv_fwd(**d, out=out)
+    torch.cuda.synchronize()
+    assert_close(out, out_cpu, "strided out")
+    assert_bits(wide_out, wide_out_cpu, "strided out incl. gaps")
+    assert_bits(d["conv_states"], ref_states, "strided states")
+
+
+@pytest.mark.parametrize("state_layout", ["dim_contiguous", "tok_contiguous"])
+@pytest.mark.parametrize("layout", ["tokens_dim", "dim_tokens"])
+def test_state_layouts_and_wider_state(state_layout, layout):
+    case = wl.varlen_prefill(801, [1, 2, 9, 200], 64, 4, num_cache_lines=6, state_len=7,
+                             layout=layout, state_layout=state_layout, has_init="bernoulli")
+    check(case)
+
+
+@pytest.mark.parametrize("layout", ["tokens_dim", "dim_tokens"])
+def test_optional_inputs_absent(layout):
+    base = dict(num_cache_lines=4, layout=layout)
+    check(wl.varlen_prefill(901, [5, 77, 2], 32, 4, use_bias=False, activation=None, **base))
+    check(wl.varlen_prefill(902, [5, 77, 2], 32, 4, has_init="null", **base))
+    check(wl.varlen_prefill(903, [5, 77, 2], 32, 4, with_cache_indices=False, **base))
+    check(wl.varlen_prefill(904, [5, 77, 2], 32, 4, with_states=False, has_init="null", **base))
+
+
+@pytest.mark.parametrize("layout", ["tokens_dim", "dim_tokens"])
+def test_invalid_indices_counted_not_faulting(layout):
+    case = wl.varlen_prefill(1001, [6, 9, 3], 16, 4, num_cache_lines=3, layout=layout,
+                             has_init="all")
+    case.cache_indices[1] = 999  # outside the pool, not the pad id
+    ref_out, ref_states, out, states, err = run_both(case, err=True)
+    assert int(err.item()) > 0
+    assert_close(out, ref_out, "invalid out")
+    assert_bits(states, ref_states, "invalid states")
+
+
+def test_large_values_and_saturation():
+    """Inputs far from the benchmark's 0.02 scale: SiLU tails, exp overflow."""
+    case = wl.varlen_prefill(1101, [40, 3], 48, 4, num_cache_lines=2, layout="tokens_dim",
+                             has_init="all", std=20.0)
+    check(case)
+
+
+def test_guard_bands_untouched():
+    """Outputs and states inside larger sentinel-filled buffers: nothing outside
+    the logical views changes."""
+    case = wl.varlen_prefill(1201, [7, 129, 2], 64, 4, num_cache_lines=4, layout="tokens_dim",
+                             has_init="bernoulli")
+    T, dim = case.total_tokens, case.dim
+    d = to_device(case.kwargs(), DEV)
+    big_out = torch.empty(T * dim + 4096, dtype=torch.bfloat16, device=DEV)
+    big_out.view(torch.int16).fill_(-777)
+    out = big_out[2048:2048 + T * dim].view(T, dim).t()
+    st = case.conv_states
+    big_st = torch.empty(st.numel() + 4096, dtype=torch.bfloat16, device=DEV)
+    big_st.view(torch.int16).fill_(-555)
+    st_view = big_st[2048:2048 + st.numel()].view(st.shape[0], st.shape[2], st.shape[1])
+    st_view.copy_(st.transpose(1, 2))
+    d["conv_states"] = st_view.transpose(1, 2)
+    ccv.ccv_fwd(**d, out=out)
+    torch.cuda.synchronize()
+    assert bool((big_out[:2048].view(torch.int16) == -777).all())
+    assert bool((big_out[2048 + T * dim:].view(torch.int16) == -777).all())
+    assert bool((big_st[:2048].view(torch.int16) == -555).all())
+    assert bool((big_st[2048 + st.numel():].view(torch.int16) == -555).all())
+    ref_states = case.conv_states.clone()
+    ref_out = sentinel_like(case.x)
+    oracle.ccv_fwd(case.x, case.weight, case.bias, ref_states, case.query_start_loc,
+                   case.cache_indices, case.has_initial_state, case.activation, -1, out=ref_out)
+    assert_close(out, ref_out, "guard out")
+    assert_bits(d["conv_states"], ref_states, "guard states")
+
+
+def test_empty_inputs_launch_nothing():
+    case = wl.varlen_prefill(1301, [0, 0], 16, 4, num_cache_lines=2)
+    check(case)
+    d = to_device(case.kwargs(), DEV)
+    d["query_start_loc"] = torch.zeros(1, dtype=torch.int32, device=DEV)
+    d["cache_indices"] = d["cache_indices"][:0]
+    d["has_initial_state"] = d["has_initial_state"][:0]
+    ccv.ccv_fwd(**d)  # batch 0
+
+
+def test_rejects_cpu_tensors_and_aliasing():
+    case = wl.varlen_prefill(1401, [4], 16, 4, num_cache_lines=1)
+    with pytest.raises(TypeError):
+        ccv.ccv_fwd(**case.kwargs())
+    d = to_device(case.kwargs(), DEV)
+    with pytest.raises(ccv.CcvError):
+        ccv.ccv_fwd(**d, out=d["x"])
+
+
+def test_cuda_graph_replay_matches_eager():
+    """Capture one call, then replay it on fresh inputs copied into the same
+    buffers: same results as an eager call on those inputs."""
+    c1 = wl.varlen_prefill(1501, [100, 3, 260], 256, 4, num_cache_lines=4, layout="tokens_dim",
+                           has_init="all")
+    c2 = wl.varlen_prefill(1502, [100, 3, 260], 256, 4, num_cache_lines=4, layout="tokens_dim",
+                           has_init="all")
+    d = to_device(c1.kwargs(), DEV)
+    out = sentinel_like(d["x"])
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        ccv.ccv_fwd(**d, out=out)  # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        ccv.ccv_fwd(**d, out=out)
+    d2 = to_device(c2.kwargs(), DEV)
+    for k in ("x", "weight", "bias", "conv_states", "query_start_loc", "cache_indices",
+              "has_initial_state"):
+        d[k].copy_(d2[k])
+    g.replay()
+    torch.cuda.synchronize()
+    ref_states = c2.conv_states.clone()
+    ref_out = sentinel_like(c2.x)
+    oracle.ccv_fwd(c2.x, c2.weight, c2.bias, ref_states, c2.query_start_loc, c2.cache_indices,
+                   c2.has_initial_state, c2.activation, -1, out=ref_out)
+    assert_close(out, ref_out, "graph out")
+    assert_bits(d["conv_states"], ref_states, "graph states")
