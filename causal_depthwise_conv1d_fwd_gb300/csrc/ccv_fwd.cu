@@ -70,14 +70,29 @@ struct ChunkInfo {
 };
 
 // Map chunk slot `slot` to its (sequence, chunk); false for a surplus slot.
+// Warp-cooperative, every lane gets the same answer.  f(i) = floor(qsl[i] /
+// chunk_tokens) + i increases strictly with i for a valid query_start_loc, so
+// {i : f(i) <= slot} is a prefix of [0, batch); each round samples 32 evenly
+// spaced candidates of the current window and keeps the 1/32 slice after the
+// last one that satisfies it: one round trip for up to 32 sequences, two for
+// up to 1024.  Garbage offsets only lead to a wrong (validated, skipped) pick.
 __device__ __forceinline__ bool locate_chunk(const FwdArgs &a, int chunk_tokens, int slot,
                                              ChunkInfo &ci) {
-    int lo = 0, hi = a.batch - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        const int f = floor_div(__ldg(a.qsl + mid), chunk_tokens) + mid;
-        if (f <= slot) lo = mid;
-        else hi = mid - 1;
+    const int lane = threadIdx.x & 31;
+    int lo = 0, n = a.batch;
+    while (n > 1) {
+        const int stride = (n + 31) >> 5;
+        const int off = lane * stride;
+        bool le = false;
+        if (off < n) {
+            const int i = lo + off;
+            le = floor_div(__ldg(a.qsl + i), chunk_tokens) + i <= slot;
+        }
+        const unsigned m = __ballot_sync(kFullMask, le);
+        if (m == 0u) break;
+        const int top = 31 - __clz(m);
+        lo += top * stride;
+        n = min(stride, n - top * stride);
     }
     const int start = __ldg(a.qsl + lo);
     const int end = __ldg(a.qsl + lo + 1);
@@ -89,6 +104,26 @@ __device__ __forceinline__ bool locate_chunk(const FwdArgs &a, int chunk_tokens,
     ci.start = start;
     ci.len = end - start;
     return true;
+}
+
+// Stage the block's weight tile (tile_c channels from cbase, W taps) and bias
+// in shared memory as [tap][channel] bf16, with coalesced global loads; every
+// thread of the block must call this (it ends with a barrier).
+template <int W>
+__device__ __forceinline__ void stage_weights(const uint16_t *w, int64_t ws_d, int64_t ws_k,
+                                              const uint16_t *bias, int dim, int cbase,
+                                              int tile_c, uint16_t *s_w, uint16_t *s_b) {
+    for (int i = threadIdx.x; i < W * tile_c; i += blockDim.x) {
+        const int cl = i / W;
+        const int k = i - cl * W;
+        const int c = cbase + cl;
+        s_w[k * tile_c + cl] = c < dim ? __ldg(w + c * ws_d + k * ws_k) : uint16_t(0);
+    }
+    for (int i = threadIdx.x; i < tile_c; i += blockDim.x) {
+        const int c = cbase + i;
+        s_b[i] = (bias != nullptr && c < dim) ? __ldg(bias + c) : uint16_t(0);
+    }
+    __syncthreads();
 }
 
 // Blocks (x < batch, y == 0) each check one sequence's indices and count
@@ -168,11 +203,15 @@ __device__ __forceinline__ void cl_token(const float (&wt)[W][VEC], const float 
 
 template <int W, bool SILU, int VEC>
 __global__ void __launch_bounds__(kThreads) fwd_cl_kernel(const FwdArgs a) {
+    constexpr int TILE_C = 32 * VEC;
+    __shared__ __align__(16) uint16_t s_w[W * TILE_C];
+    __shared__ __align__(16) uint16_t s_b[TILE_C];
     validate_sequence(a);
     ChunkInfo ci;
     if (!locate_chunk(a, kClChunk, blockIdx.x, ci)) return;
     int line;
     if (!sequence_line(a, ci, line)) return;
+    stage_weights<W>(a.w, a.ws_d, a.ws_k, a.bias, a.dim, blockIdx.y * TILE_C, TILE_C, s_w, s_b);
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -190,11 +229,9 @@ __global__ void __launch_bounds__(kThreads) fwd_cl_kernel(const FwdArgs a) {
 
     float wt[W][VEC], bs[VEC];
 #pragma unroll
-    for (int v = 0; v < VEC; ++v) {
-#pragma unroll
-        for (int k = 0; k < W; ++k) wt[k][v] = bf16_bits(__ldg(a.w + (c0 + v) * a.ws_d + k * a.ws_k));
-        bs[v] = a.bias ? bf16_bits(__ldg(a.bias + c0 + v)) : 0.0f;
-    }
+    for (int k = 0; k < W; ++k)
+        reinterpret_cast<const Raw<VEC> *>(s_w + k * TILE_C)[lane].to_float(wt[k]);
+    reinterpret_cast<const Raw<VEC> *>(s_b)[lane].to_float(bs);
 
     float ring[W - 1][VEC];
     if (ci.chunk == 0 && warp == 0) {

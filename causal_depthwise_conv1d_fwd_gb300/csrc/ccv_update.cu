@@ -6,9 +6,9 @@
 // the state left and append the new inputs, STEPS 3-5 bias, weights and the
 // token loop), non-speculative path.
 //
-// One thread owns 8 consecutive channels (16-byte vectors) of one batch row;
-// the grid is batch x ceil(dim / 1024) blocks, fixed by the sizes, so a CUDA
-// graph replays it unchanged.  Every element of the state line and of out is
+// One thread owns 8 consecutive channels (16-byte vectors) of 4 consecutive
+// batch rows; the grid is ceil(batch / 4) x ceil(dim / 1024) blocks, fixed by
+// the sizes, so a CUDA graph replays it unchanged.  Every element of the state line and of out is
 // read and written by the same thread, which makes the in-place state shift
 // and out == x (the page's wrapper writes the output over x) hazard-free.
 #include "ccv_common.cuh"
@@ -17,6 +17,7 @@ namespace ccv {
 namespace {
 
 constexpr int kThreads = 128;
+constexpr int kRows = 4;  // batch rows per block
 
 struct UpdArgs {
     const uint16_t *x;
@@ -58,64 +59,140 @@ __device__ __forceinline__ void scatter(uint16_t *p, int64_t stride, bool vec, c
     }
 }
 
+// Stage the block's weights and bias as [tap][channel] bf16 in shared memory
+// with coalesced loads; every thread of the block calls this.
+template <int W>
+__device__ __forceinline__ void stage_weights(const UpdArgs &a, int cbase, int tile_c,
+                                              uint16_t *s_w, uint16_t *s_b) {
+    for (int i = threadIdx.x; i < W * tile_c; i += blockDim.x) {
+        const int cl = i / W;
+        const int k = i - cl * W;
+        const int c = cbase + cl;
+        s_w[k * tile_c + cl] = c < a.dim ? __ldg(a.w + c * a.ws_d + k * a.ws_k) : uint16_t(0);
+    }
+    for (int i = threadIdx.x; i < tile_c; i += blockDim.x) {
+        const int c = cbase + i;
+        s_b[i] = (a.bias != nullptr && c < a.dim) ? __ldg(a.bias + c) : uint16_t(0);
+    }
+    __syncthreads();
+}
+
+template <int W, bool SILU, int VEC>
+__device__ __forceinline__ void conv_token(const float (&wt)[W][VEC], const float (&bs)[VEC],
+                                           const float (&ring)[W - 1][VEC], const float (&xf)[VEC],
+                                           Raw<VEC> &o) {
+    float acc[VEC];
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) {
+        float s = bs[v];
+#pragma unroll
+        for (int k = 0; k < W - 1; ++k) s = fmaf(wt[k][v], ring[k][v], s);
+        s = fmaf(wt[W - 1][v], xf[v], s);
+        acc[v] = SILU ? silu(s) : s;
+    }
+    o.from_float(acc);
+}
+
+// A block covers kThreads*VEC channels of kRows consecutive batch rows, so the
+// weights it stages serve kRows rows.
 template <int W, bool SILU, int VEC>
 __global__ void __launch_bounds__(kThreads) update_kernel(const UpdArgs a) {
-    const int b = blockIdx.x / a.ctiles;
-    const int ct = blockIdx.x - b * a.ctiles;
-    const int c0 = (ct * kThreads + threadIdx.x) * VEC;
+    constexpr int TILE_C = kThreads * VEC;
+    __shared__ __align__(16) uint16_t s_w[W * TILE_C];
+    __shared__ __align__(16) uint16_t s_b[TILE_C];
+    const int rg = blockIdx.x / a.ctiles;
+    const int ct = blockIdx.x - rg * a.ctiles;
+    stage_weights<W>(a, ct * TILE_C, TILE_C, s_w, s_b);
+    const int c0 = ct * TILE_C + threadIdx.x * VEC;
     if (c0 >= a.dim) return;
-    const int line = a.idx ? __ldg(a.idx + b) : b;
-    if (line == a.pad) return;
-    if (line < 0 || line >= a.num_lines) {
-        if (c0 == 0) count_error(a.err);
-        return;
-    }
 
     float wt[W][VEC], bs[VEC];
 #pragma unroll
-    for (int v = 0; v < VEC; ++v) {
+    for (int k = 0; k < W; ++k)
+        reinterpret_cast<const Raw<VEC> *>(s_w + k * TILE_C)[threadIdx.x].to_float(wt[k]);
+    reinterpret_cast<const Raw<VEC> *>(s_b)[threadIdx.x].to_float(bs);
+
+    // Resolve the rows' state lines (skipped rows get line -1).
+    int lines[kRows];
 #pragma unroll
-        for (int k = 0; k < W; ++k) wt[k][v] = bf16_bits(__ldg(a.w + (c0 + v) * a.ws_d + k * a.ws_k));
-        bs[v] = a.bias ? bf16_bits(__ldg(a.bias + c0 + v)) : 0.0f;
+    for (int r = 0; r < kRows; ++r) {
+        const int b = rg * kRows + r;
+        int line = -1;
+        if (b < a.batch) {
+            line = a.idx ? __ldg(a.idx + b) : b;
+            if (line == a.pad) {
+                line = -1;
+            } else if (line < 0 || line >= a.num_lines) {
+                if (c0 == 0) count_error(a.err);
+                line = -1;
+            }
+        }
+        lines[r] = line;
     }
 
-    uint16_t *sp = a.st + line * a.ss_l + c0 * a.ss_d;
-    Raw<VEC> win[W - 1];
+    if (a.seqlen == 1) {
+        // Issue every row's window and input before any arithmetic.
+        Raw<VEC> win[kRows][W - 1], xv[kRows];
 #pragma unroll
-    for (int j = 0; j < W - 1; ++j) win[j] = gather<VEC>(sp + j * a.ss_t, a.ss_d, a.st_vec);
-    float ring[W - 1][VEC];
+        for (int r = 0; r < kRows; ++r) {
+            if (lines[r] < 0) continue;
+            const uint16_t *sp = a.st + lines[r] * a.ss_l + c0 * a.ss_d;
 #pragma unroll
-    for (int j = 0; j < W - 1; ++j) win[j].to_float(ring[j]);
-    // The state keeps everything but its oldest column: columns 0..W-3 take
-    // the old columns 1..W-2; the new inputs go to columns W-2 onwards.
-#pragma unroll
-    for (int j = 0; j + 1 < W - 1; ++j) scatter<VEC>(sp + j * a.ss_t, a.ss_d, a.st_vec, win[j + 1]);
-
-    const uint16_t *xp = a.x + b * a.xs_b + c0 * a.xs_d;
-    uint16_t *op = a.out + b * a.os_b + c0 * a.os_d;
-    for (int t = 0; t < a.seqlen; ++t) {
-        const Raw<VEC> xv = gather<VEC>(xp + t * a.xs_t, a.xs_d, a.x_vec);
-        float xf[VEC];
-        xv.to_float(xf);
-        float acc[VEC];
-#pragma unroll
-        for (int v = 0; v < VEC; ++v) {
-            float s = bs[v];
-#pragma unroll
-            for (int k = 0; k < W - 1; ++k) s = fmaf(wt[k][v], ring[k][v], s);
-            s = fmaf(wt[W - 1][v], xf[v], s);
-            acc[v] = SILU ? silu(s) : s;
+            for (int j = 0; j < W - 1; ++j) win[r][j] = gather<VEC>(sp + j * a.ss_t, a.ss_d, a.st_vec);
+            const int b = rg * kRows + r;
+            xv[r] = gather<VEC>(a.x + b * a.xs_b + c0 * a.xs_d, a.xs_d, a.x_vec);
         }
-        Raw<VEC> o;
-        o.from_float(acc);
-        scatter<VEC>(op + t * a.os_t, a.os_d, a.o_vec, o);
-        scatter<VEC>(sp + (W - 2 + t) * a.ss_t, a.ss_d, a.st_vec, xv);
 #pragma unroll
-        for (int k = 0; k < W - 2; ++k)
+        for (int r = 0; r < kRows; ++r) {
+            if (lines[r] < 0) continue;
+            const int b = rg * kRows + r;
+            uint16_t *sp = a.st + lines[r] * a.ss_l + c0 * a.ss_d;
+            float ring[W - 1][VEC], xf[VEC];
 #pragma unroll
-            for (int v = 0; v < VEC; ++v) ring[k][v] = ring[k + 1][v];
+            for (int j = 0; j < W - 1; ++j) win[r][j].to_float(ring[j]);
+            xv[r].to_float(xf);
+            Raw<VEC> o;
+            conv_token<W, SILU, VEC>(wt, bs, ring, xf, o);
+            scatter<VEC>(a.out + b * a.os_b + c0 * a.os_d, a.os_d, a.o_vec, o);
+            // The state keeps all but its oldest column and appends the input.
 #pragma unroll
-        for (int v = 0; v < VEC; ++v) ring[W - 2][v] = xf[v];
+            for (int j = 0; j + 1 < W - 1; ++j) scatter<VEC>(sp + j * a.ss_t, a.ss_d, a.st_vec, win[r][j + 1]);
+            scatter<VEC>(sp + (W - 2) * a.ss_t, a.ss_d, a.st_vec, xv[r]);
+        }
+        return;
+    }
+
+    for (int r = 0; r < kRows; ++r) {
+        if (lines[r] < 0) continue;
+        const int b = rg * kRows + r;
+        uint16_t *sp = a.st + lines[r] * a.ss_l + c0 * a.ss_d;
+        Raw<VEC> win[W - 1];
+#pragma unroll
+        for (int j = 0; j < W - 1; ++j) win[j] = gather<VEC>(sp + j * a.ss_t, a.ss_d, a.st_vec);
+        float ring[W - 1][VEC];
+#pragma unroll
+        for (int j = 0; j < W - 1; ++j) win[j].to_float(ring[j]);
+        // Columns 0..W-3 take the old columns 1..W-2; the new inputs go to
+        // columns W-2 onwards.
+#pragma unroll
+        for (int j = 0; j + 1 < W - 1; ++j) scatter<VEC>(sp + j * a.ss_t, a.ss_d, a.st_vec, win[j + 1]);
+        const uint16_t *xp = a.x + b * a.xs_b + c0 * a.xs_d;
+        uint16_t *op = a.out + b * a.os_b + c0 * a.os_d;
+        for (int t = 0; t < a.seqlen; ++t) {
+            const Raw<VEC> xr = gather<VEC>(xp + t * a.xs_t, a.xs_d, a.x_vec);
+            float xf[VEC];
+            xr.to_float(xf);
+            Raw<VEC> o;
+            conv_token<W, SILU, VEC>(wt, bs, ring, xf, o);
+            scatter<VEC>(op + t * a.os_t, a.os_d, a.o_vec, o);
+            scatter<VEC>(sp + (W - 2 + t) * a.ss_t, a.ss_d, a.st_vec, xr);
+#pragma unroll
+            for (int k = 0; k < W - 2; ++k)
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) ring[k][v] = ring[k + 1][v];
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) ring[W - 2][v] = xf[v];
+        }
     }
 }
 
@@ -196,7 +273,7 @@ extern "C" int ccv_update(const void *x, int64_t x_stride_b, int64_t x_stride_di
     a.st_vec = vec && s_stride_dim == 1 && aligned16(conv_state) && s_stride_line % 8 == 0 &&
                s_stride_tok % 8 == 0;
     a.ctiles = (dim + kThreads * vw - 1) / (kThreads * vw);
-    const int64_t blocks = static_cast<int64_t>(batch) * a.ctiles;
+    const int64_t blocks = static_cast<int64_t>((batch + kRows - 1) / kRows) * a.ctiles;
     if (blocks > 0x7fffffffLL) return CCV_ERR_SIZE;
     KernelFn fn = vec ? pick_kernel<8>(width, silu != 0) : pick_kernel<1>(width, silu != 0);
     fn<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(a);

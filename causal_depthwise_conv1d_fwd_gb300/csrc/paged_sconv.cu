@@ -25,7 +25,7 @@ namespace {
 
 constexpr int kThreads = 128;
 constexpr int kWarps = kThreads / 32;
-constexpr int kRun = 16;  // tokens per warp
+constexpr int kRun = 16;  // tokens per warp (at most 32: one lane plans each)
 constexpr int kBlockTokens = kWarps * kRun;
 
 struct PagedArgs {
@@ -49,108 +49,187 @@ struct PagedArgs {
     int *err;
 };
 
+// Tap source kinds, two bits per tap in TokenPlan::kinds.
+constexpr int kTapZero = 0;    // PAD row or a position before 0: contributes nothing
+constexpr int kTapX = 1;       // in this forward: x row (t - (W-1) + iw)
+constexpr int kTapCache = 2;   // before this forward: cache entry at TokenPlan::off[iw]
+
+// What every channel of a token needs: where each tap comes from, and where
+// the token's input goes (ins < 0: nowhere).  Offsets exclude the channel's
+// head and D offset, which each thread adds.
+template <int W>
+struct TokenPlan {
+    int kinds;
+    int64_t off[W];
+    int64_t ins;
+};
+
+// Lane l of a warp resolves the plan of token t (one lane per token), so the
+// per-token index loads and block-table lookups are issued once per warp and
+// overlap across the warp's tokens.
+template <int W>
+__device__ __forceinline__ TokenPlan<W> plan_token(const PagedArgs &a, int t) {
+    TokenPlan<W> p;
+    p.kinds = 0;
+    p.ins = -1;
+#pragma unroll
+    for (int iw = 0; iw < W; ++iw) p.off[iw] = 0;
+    const int64_t slot = __ldg(a.slot + t);
+    if (slot < 0) return p;  // PAD row: every tap is zero, nothing is inserted
+    const int64_t pos = __ldg(a.pos + t);
+    const int req = __ldg(a.seq_idx + t);
+    const int qs = __ldg(a.qstart + t);
+    const int64_t blk = slot / a.N;
+    if (blk < a.num_blocks) p.ins = blk * a.cs_blk + (slot % a.N) * a.cs_n;
+    else count_error(a.err);
+#pragma unroll
+    for (int iw = 0; iw < W; ++iw) {
+        const int64_t src = pos - (W - 1) + iw;
+        const int row = t - (W - 1) + iw;
+        if (src < 0) continue;
+        if (row >= qs) {
+            if (row < 0) {
+                count_error(a.err);
+                continue;
+            }
+            p.kinds |= kTapX << (2 * iw);
+            continue;
+        }
+        int64_t lblk = src / a.N;
+        if (lblk > a.max_blocks - 1) lblk = a.max_blocks - 1;
+        if (req < 0 || req >= a.bt_rows) {
+            count_error(a.err);
+            continue;
+        }
+        const int64_t pb = __ldg(a.bt + req * a.bt_r + lblk);
+        if (pb < 0 || pb >= a.num_blocks) {
+            count_error(a.err);
+            continue;
+        }
+        p.kinds |= kTapCache << (2 * iw);
+        p.off[iw] = pb * a.cs_blk + (src % a.N) * a.cs_n;
+    }
+    return p;
+}
+
+__device__ __forceinline__ int64_t shfl64(int64_t v, int src) {
+    const int lo = __shfl_sync(kFullMask, static_cast<int>(v & 0xffffffffLL), src);
+    const int hi = __shfl_sync(kFullMask, static_cast<int>(v >> 32), src);
+    return (static_cast<int64_t>(hi) << 32) | static_cast<uint32_t>(lo);
+}
+
 template <int W, bool SILU, bool RESID, int VEC>
 __global__ void __launch_bounds__(kThreads) paged_kernel(const PagedArgs a) {
+    constexpr int TILE_C = 32 * VEC;
+    constexpr int G = 8;  // x rows loaded together
+    __shared__ __align__(16) uint16_t s_w[W * TILE_C];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    const int c0 = (blockIdx.y * 32 + lane) * VEC;
-    if (c0 >= a.C) return;
+    const int cbase = blockIdx.y * TILE_C;
+    for (int i = threadIdx.x; i < W * TILE_C; i += kThreads) {
+        const int cl = i / W;
+        const int k = i - cl * W;
+        const int c = cbase + cl;
+        s_w[k * TILE_C + cl] = c < a.C ? __ldg(a.w + c * a.ws_c + k * a.ws_k) : uint16_t(0);
+    }
+    __syncthreads();
+
     const int t0 = blockIdx.x * kBlockTokens + warp * kRun;
     const int t1 = min(t0 + kRun, a.T);
-    if (t0 >= t1) return;
-
-    const int head = c0 / a.ws;
-    const int cd = a.off_s + c0 % a.ws;
-    const int64_t head_off = static_cast<int64_t>(head) * a.cs_h + cd;
+    if (t0 >= t1) return;  // warp-uniform
+    const int c0 = cbase + lane * VEC;
+    const bool active = c0 < a.C;  // inactive lanes still take part in the shuffles
 
     float wt[W][VEC];
 #pragma unroll
-    for (int v = 0; v < VEC; ++v)
+    for (int k = 0; k < W; ++k)
+        reinterpret_cast<const Raw<VEC> *>(s_w + k * TILE_C)[lane].to_float(wt[k]);
+
+    TokenPlan<W> mine;
+    mine.kinds = 0;
+    mine.ins = -1;
 #pragma unroll
-        for (int k = 0; k < W; ++k) wt[k][v] = bf16_bits(__ldg(a.w + (c0 + v) * a.ws_c + k * a.ws_k));
+    for (int iw = 0; iw < W; ++iw) mine.off[iw] = 0;
+    if (t0 + lane < t1) mine = plan_token<W>(a, t0 + lane);
+
+    const int head = active ? c0 / a.ws : 0;
+    const int64_t chan_off = static_cast<int64_t>(head) * a.cs_h + a.off_s + (active ? c0 % a.ws : 0);
 
     // ring[m] holds x row (t - (W-1) + m) for the token t being processed.
     float ring[W - 1][VEC];
 #pragma unroll
     for (int m = 0; m < W - 1; ++m) {
         const int row = t0 - (W - 1) + m;
-        if (row >= 0) load_plain<VEC>(a.x + row * a.xs_t + c0).to_float(ring[m]);
+        if (active && row >= 0) load_plain<VEC>(a.x + row * a.xs_t + c0).to_float(ring[m]);
         else
 #pragma unroll
             for (int v = 0; v < VEC; ++v) ring[m][v] = 0.0f;
     }
 
-    for (int t = t0; t < t1; ++t) {
-        const int64_t slot = __ldg(a.slot + t);
-        const int64_t pos = __ldg(a.pos + t);
-        const int req = __ldg(a.seq_idx + t);
-        const int qs = __ldg(a.qstart + t);
-        const Raw<VEC> xr = load_stream<VEC>(a.x + t * a.xs_t + c0);
-        float xf[VEC];
-        xr.to_float(xf);
-        const bool real = slot >= 0;
-
-        // Part 1: insert this token's input at its slot.
-        if (real) {
-            const int64_t blk = slot / a.N;
-            if (blk < a.num_blocks) {
-                uint16_t *dst = a.cache + blk * a.cs_blk + (slot % a.N) * a.cs_n + head_off;
-                store_plain<VEC>(dst, xr);
-            } else if (c0 == 0) {
-                count_error(a.err);
-            }
+    for (int g = t0; g < t1; g += G) {
+        Raw<VEC> xg[G];
+#pragma unroll
+        for (int u = 0; u < G; ++u) {
+            if (active && g + u < t1) xg[u] = load_stream<VEC>(a.x + (g + u) * a.xs_t + c0);
+            else xg[u].zero();
         }
+#pragma unroll
+        for (int u = 0; u < G; ++u) {
+            const int t = g + u;
+            if (t >= t1) break;  // warp-uniform
+            const int src_lane = t - t0;
+            const int kinds = __shfl_sync(kFullMask, mine.kinds, src_lane);
+            int64_t off[W];
+#pragma unroll
+            for (int iw = 0; iw < W; ++iw) off[iw] = shfl64(mine.off[iw], src_lane);
+            const int64_t ins = shfl64(mine.ins, src_lane);
 
-        // Part 2: the W taps ending at this token's absolute position.
-        float acc[VEC];
+            float xf[VEC];
+            xg[u].to_float(xf);
+            if (active && ins >= 0) store_plain<VEC>(a.cache + ins + chan_off, xg[u]);
+
+            Raw<VEC> cached[W];
 #pragma unroll
-        for (int v = 0; v < VEC; ++v) acc[v] = 0.0f;
+            for (int iw = 0; iw < W; ++iw) {
+                if (active && ((kinds >> (2 * iw)) & 3) == kTapCache)
+                    cached[iw] = load_plain<VEC>(a.cache + off[iw] + chan_off);
+                else
+                    cached[iw].zero();
+            }
+            float acc[VEC];
 #pragma unroll
-        for (int iw = 0; iw < W; ++iw) {
-            const int64_t src = pos - (W - 1) + iw;
-            const int row = t - (W - 1) + iw;
-            if (!real || src < 0) continue;
-            float tap[VEC];
-            if (row >= qs) {
-                if (row < 0) {
-                    if (c0 == 0) count_error(a.err);
-                    continue;
+            for (int v = 0; v < VEC; ++v) acc[v] = 0.0f;
+#pragma unroll
+            for (int iw = 0; iw < W; ++iw) {
+                const int kind = (kinds >> (2 * iw)) & 3;
+                if (kind == kTapZero) continue;
+                float tap[VEC];
+                if (kind == kTapX) {
+#pragma unroll
+                    for (int v = 0; v < VEC; ++v) tap[v] = iw == W - 1 ? xf[v] : ring[iw][v];
+                } else {
+                    cached[iw].to_float(tap);
                 }
 #pragma unroll
-                for (int v = 0; v < VEC; ++v) tap[v] = iw == W - 1 ? xf[v] : ring[iw][v];
-            } else {
-                int64_t lblk = src / a.N;
-                if (lblk > a.max_blocks - 1) lblk = a.max_blocks - 1;
-                if (req < 0 || req >= a.bt_rows) {
-                    if (c0 == 0) count_error(a.err);
-                    continue;
-                }
-                const int64_t blk = __ldg(a.bt + req * a.bt_r + lblk);
-                if (blk < 0 || blk >= a.num_blocks) {
-                    if (c0 == 0) count_error(a.err);
-                    continue;
-                }
-                load_plain<VEC>(a.cache + blk * a.cs_blk + (src % a.N) * a.cs_n + head_off)
-                    .to_float(tap);
+                for (int v = 0; v < VEC; ++v) acc[v] = fmaf(tap[v], wt[iw][v], acc[v]);
             }
 #pragma unroll
-            for (int v = 0; v < VEC; ++v) acc[v] = fmaf(tap[v], wt[iw][v], acc[v]);
+            for (int v = 0; v < VEC; ++v) {
+                if (SILU) acc[v] = silu(acc[v]);
+                if (RESID) acc[v] = acc[v] + xf[v];
+            }
+            if (active) {
+                Raw<VEC> o;
+                o.from_float(acc);
+                store_stream<VEC>(a.out + t * a.os_t + c0, o);
+            }
+#pragma unroll
+            for (int m = 0; m < W - 2; ++m)
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) ring[m][v] = ring[m + 1][v];
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) ring[W - 2][v] = xf[v];
         }
-#pragma unroll
-        for (int v = 0; v < VEC; ++v) {
-            if (SILU) acc[v] = silu(acc[v]);
-            if (RESID) acc[v] = acc[v] + xf[v];
-        }
-        Raw<VEC> o;
-        o.from_float(acc);
-        store_stream<VEC>(a.out + t * a.os_t + c0, o);
-
-#pragma unroll
-        for (int m = 0; m < W - 2; ++m)
-#pragma unroll
-            for (int v = 0; v < VEC; ++v) ring[m][v] = ring[m + 1][v];
-#pragma unroll
-        for (int v = 0; v < VEC; ++v) ring[W - 2][v] = xf[v];
     }
 }
 
