@@ -319,7 +319,7 @@ def make_parts(dev, rank):
         out = torch.empty_strided(d["x"].shape, d["x"].stride(), dtype=torch.bfloat16, device=dev)
         dev_args[name] = (d, out)
         launch = ccv.prepare_ccv_fwd(**d, out=out)
-        parts.append(Part(name, "fwd_cl_kernel" if name.endswith("tokens_dim") else "fwd_cf_kernel",
+        parts.append(Part(name, "fwd_cl_async_kernel" if name.endswith("tokens_dim") else "fwd_cf_async_kernel",
                           1, prefill_bytes(c), prefill_tokens(c),
                           (lambda launch=launch: launch(stream))))
     c = cases["decode"]

@@ -136,4 +136,49 @@ inline Extent extent_of(const void *p, int64_t n0, int64_t s0, int64_t n1, int64
 }
 inline bool overlaps(const Extent &a, const Extent &b) { return a.lo <= b.hi && b.lo <= a.hi; }
 
+constexpr int kMaxDevices = 64;
+
+// Streaming multiprocessors of the current device (cached per device).
+inline int current_device_sms(int *device_out = nullptr) {
+    static int cache[kMaxDevices] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+    if (device_out) *device_out = dev;
+    if (dev < 0 || dev >= kMaxDevices) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        return n > 0 ? n : 1;
+    }
+    if (cache[dev] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cache[dev] = n > 0 ? n : 1;
+    }
+    return cache[dev];
+}
+
+// Prepare `fn` to run with `threads` threads and `bytes` of dynamic shared
+// memory on the current device and return how many of its blocks fit on one
+// SM (0 on error, with *err set).  The attribute and the occupancy are
+// computed once per (kernel, device) and cached, so later calls -- including
+// ones made while a CUDA graph is being captured -- only read the cache.
+template <auto kKernel>
+inline int resident_blocks(int threads, size_t bytes, int dev, cudaError_t *err) {
+    static int cache[kMaxDevices] = {0};  // one cache per kernel instantiation
+    const auto fn = kKernel;
+    *err = cudaSuccess;
+    const bool cacheable = dev >= 0 && dev < kMaxDevices;
+    if (cacheable && cache[dev] > 0) return cache[dev];
+    cudaError_t e =
+        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+    int blocks = 0;
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, fn, threads, bytes);
+    if (e != cudaSuccess || blocks <= 0) {
+        *err = e != cudaSuccess ? e : cudaErrorInvalidConfiguration;
+        return 0;
+    }
+    if (cacheable) cache[dev] = blocks;
+    return blocks;
+}
+
 }  // namespace ccv

@@ -29,6 +29,8 @@
 // Accumulation is fp32 in the pages' order (bias first, taps 0..W-1), SiLU
 // in fp32, one round-to-nearest-even store to bf16.
 #include "ccv_common.cuh"
+#include "ccv_math2.cuh"
+#include "ccv_pipeline.cuh"
 
 namespace ccv {
 namespace {
@@ -423,6 +425,405 @@ __global__ void __launch_bounds__(kThreads) fwd_cf_kernel(const FwdArgs a) {
     }
 }
 
+// ------------------------------------------ channel-last, cp.async ----
+//
+// One block owns one (sequence chunk of kCaChunk tokens, 256-channel tile);
+// warp w takes the chunk's w-th run of kCaRun tokens, lane l channels
+// 8l..8l+7 of the tile.  Each thread streams its rows through a private ring
+// of kCaSlots 16-byte shared-memory slots with cp.async, keeping kCaSlots-1
+// rows in flight at no register cost, and reads back only what it copied
+// (so no barrier is needed).  The row loop is unrolled by the ring size so
+// slot offsets are constants and the W-1 previous rows are renamed rather
+// than moved.  Weights stay packed bf16x2 and feed native mixed-precision
+// bf16 x bf16 + fp32 FMAs (one rounding, the same value as the fp32 fma of
+// the widened operands); the bias enters through the first tap.  The first
+// run of a sequence takes its prior from conv_state, the others from the W-1
+// rows before the run.
+
+constexpr int kCaThreads = 256;
+constexpr int kCaWarps = kCaThreads / 32;
+constexpr int kCaRun = 32;
+constexpr int kCaChunk = kCaWarps * kCaRun;
+constexpr int kCaSlots = 16;
+constexpr int kCaTileC = 256;
+constexpr size_t kCaSmem = sizeof(uint4) * kCaSlots * kCaThreads;  // dynamic: the slot rings
+
+__device__ __forceinline__ uint4 load8_state(const FwdArgs &a, int line, int c0, int col) {
+    const uint16_t *p = a.st + line * a.ss_l + c0 * a.ss_d + col * a.ss_t;
+    if (a.st_vec) return *reinterpret_cast<const uint4 *>(p);
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) w[q] = uint32_t(p[(2 * q) * a.ss_d]) | (uint32_t(p[(2 * q + 1) * a.ss_d]) << 16);
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__device__ __forceinline__ void store8_state(const FwdArgs &a, int line, int c0, int col, uint4 v) {
+    uint16_t *p = a.st + line * a.ss_l + c0 * a.ss_d + col * a.ss_t;
+    if (a.st_vec) {
+        *reinterpret_cast<uint4 *>(p) = v;
+        return;
+    }
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        p[(2 * q) * a.ss_d] = uint16_t(w[q] & 0xffffu);
+        p[(2 * q + 1) * a.ss_d] = uint16_t(w[q] >> 16);
+    }
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4 &v, int q) {
+    return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
+}
+
+// One output row of 8 channels: taps over ring[0..W-2] (oldest first) and v.
+template <int W, bool SILU>
+__device__ __forceinline__ uint4 ca_row(const uint4 (&wpk)[W], const float (&bs)[8],
+                                        const uint4 (&ring)[W - 1], const uint4 &v) {
+    float acc[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        fma_bf16x2_init(acc[2 * q], acc[2 * q + 1], word_of(ring[0], q), word_of(wpk[0], q),
+                        bs[2 * q], bs[2 * q + 1]);
+#pragma unroll
+    for (int k = 1; k < W; ++k) {
+        const uint4 &u = k < W - 1 ? ring[k < W - 1 ? k : 0] : v;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) fma_bf16x2(acc[2 * q], acc[2 * q + 1], word_of(u, q), word_of(wpk[k], q));
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        f32x2 r = pack2(acc[2 * q], acc[2 * q + 1]);
+        if (SILU) r = silu2(r);
+        o[q] = f32x2_to_bf16x2(r);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+template <int W, bool SILU>
+__global__ void __launch_bounds__(kCaThreads, 3) fwd_cl_async_kernel(const FwdArgs a) {
+    extern __shared__ __align__(16) uint4 s_ring[];  // [kCaSlots][kCaThreads]
+    __shared__ __align__(16) uint16_t s_w[W * kCaTileC];
+    __shared__ __align__(16) uint16_t s_b[kCaTileC];
+    validate_sequence(a);
+    ChunkInfo ci;
+    if (!locate_chunk(a, kCaChunk, blockIdx.x, ci)) return;
+    int line;
+    if (!sequence_line(a, ci, line)) return;
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int c0 = blockIdx.y * kCaTileC + lane * 8;
+    const int cbeg = ci.start + ci.chunk * kCaChunk;
+    const int cend = ci.start + min(ci.len, (ci.chunk + 1) * kCaChunk);
+    const int r0 = cbeg + warp * kCaRun;
+    const int r1 = min(r0 + kCaRun, cend);
+    const bool first = ci.chunk == 0 && warp == 0;
+    const int h = first ? 0 : W - 1;  // halo rows streamed before the run
+    const int row_base = r0 - h;
+    const int nrows = r1 > r0 ? r1 - row_base : 0;
+    const bool active = c0 < a.dim && nrows > 0;
+    const int64_t xs = a.xs_t;
+    const uint16_t *src = a.x + c0 + row_base * xs;
+    uint4 *ring_base = s_ring + tid;
+
+    // Start the stream before anything else; slot j % kCaSlots holds row j.
+#pragma unroll
+    for (int j = 0; j < kCaSlots - 1; ++j) {
+        if (active && j < nrows) cp_async16(ring_base + j * kCaThreads, src + j * xs);
+        cp_async_commit();
+    }
+    stage_weights<W>(a.w, a.ws_d, a.ws_k, a.bias, a.dim, blockIdx.y * kCaTileC, kCaTileC, s_w, s_b);
+    if (!active) return;
+
+    uint4 wpk[W];
+#pragma unroll
+    for (int k = 0; k < W; ++k) wpk[k] = reinterpret_cast<const uint4 *>(s_w + k * kCaTileC)[lane];
+    float bs[8];
+    reinterpret_cast<const Raw<8> *>(s_b)[lane].to_float(bs);
+
+    uint4 ring[W - 1];
+    if (first) {
+        uint4 prior[W - 1];
+        const bool init = a.st != nullptr && a.has_init != nullptr && a.has_init[ci.seq] != 0;
+#pragma unroll
+        for (int j = 0; j < W - 1; ++j) {
+            prior[j] = init ? load8_state(a, line, c0, j) : make_uint4(0u, 0u, 0u, 0u);
+            ring[j] = prior[j];
+        }
+        if (a.st != nullptr) {
+            // New state = last W-1 entries of prior ++ x[sequence].
+            uint4 nw[W - 1];
+#pragma unroll
+            for (int j = 0; j < W - 1; ++j) {
+                const int idx = ci.len + j;
+                if (idx < W - 1) {
+#pragma unroll
+                    for (int q = 0; q < W - 1; ++q)
+                        if (q == idx) nw[j] = prior[q];
+                } else {
+                    nw[j] = *reinterpret_cast<const uint4 *>(a.x + c0 + (ci.start + idx - (W - 1)) * xs);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < W - 1; ++j) store8_state(a, line, c0, j, nw[j]);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < W - 1; ++j) ring[j] = make_uint4(0u, 0u, 0u, 0u);
+    }
+
+    const int64_t os = a.os_t;
+    uint16_t *dst = a.out + c0 + row_base * os;
+    const uint16_t *nxt = src + (kCaSlots - 1) * xs;  // next row to stream in
+    // One row: wait for it, refill the slot read in the previous step, compute.
+    auto step = [&](int j, int slot) {
+        cp_async_wait<kCaSlots - 2>();
+        const uint4 v = ring_base[slot * kCaThreads];
+        if (j + kCaSlots - 1 < nrows)
+            cp_async16(ring_base + ((slot + kCaSlots - 1) % kCaSlots) * kCaThreads, nxt);
+        cp_async_commit();
+        nxt += xs;
+        if (j >= h) __stcs(reinterpret_cast<uint4 *>(dst), ca_row<W, SILU>(wpk, bs, ring, v));
+        dst += os;
+#pragma unroll
+        for (int k = 0; k < W - 2; ++k) ring[k] = ring[k + 1];
+        ring[W - 2] = v;
+    };
+    int j = 0;
+    for (; j + kCaSlots <= nrows; j += kCaSlots) {
+#pragma unroll
+        for (int u = 0; u < kCaSlots; ++u) step(j + u, u);
+    }
+    for (int u = 0; j < nrows; ++j, ++u) step(j, u);
+}
+
+// ----------------------------------------- channel-first, cp.async ----
+//
+// One warp owns one channel row of one sequence chunk of kCfaChunk tokens (a
+// block holds kCfaWarps consecutive rows).  The chunk is kCfaSegs warp-wide
+// segments of 256 tokens that start at the row's 16-byte boundary at or
+// before the first token needed (the chunk length leaves room for the halo
+// and the alignment); lane l owns tokens 8l..8l+7 of a segment.  Each lane
+// streams its 16-byte vectors through a private ring of kCfaSlots
+// shared-memory slots with cp.async, started as soon as the chunk is known (a
+// vector that crosses the chunk's edge is assembled with scalar loads, the
+// prior included, and stored into the slot instead).  The 4 tokens before a
+// lane's vector come from lane l-1 by shuffle (lane 0: lane 31 of the
+// previous segment).  Taps are scalar fp32 FMAs on the widened 12-token
+// window; segments wholly inside the chunk run without per-lane checks.
+
+constexpr int kCfaThreads = 256;
+constexpr int kCfaWarps = kCfaThreads / 32;
+constexpr int kCfaSegs = 32;
+constexpr int kCfaChunk = kCfaSegs * 256 - 16;  // + halo (<= 4) + alignment (<= 7) fits the segments
+constexpr int kCfaSlots = 8;
+constexpr size_t kCfaSmem = sizeof(uint4) * kCfaSlots * kCfaThreads;
+static_assert(kCfaChunk + kMaxWidth - 1 + 7 <= kCfaSegs * 256, "a chunk must fit its segments");
+
+// The 8 logical inputs at tokens t0..t0+7 of one row: x inside [lo, cend),
+// the prior (packed, oldest first) just before a sequence's first chunk, 0
+// elsewhere.  Only vectors at a chunk's edges take this path.
+template <int W>
+__device__ __noinline__ uint4 cfa_edge_vector(const uint16_t *xc, int t0, int lo, int cbeg, int cend,
+                                              bool chunk0, uint32_t prior01, uint32_t prior23) {
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t pair = 0;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int t = t0 + 2 * q + e;
+            uint32_t val = 0;
+            if (t >= lo && t < cend) {
+                val = xc[t];
+            } else if (chunk0 && t >= cbeg - (W - 1) && t < cbeg) {
+                const int i = t - cbeg + (W - 1);  // prior column
+                const uint32_t src = i < 2 ? prior01 : prior23;
+                val = (i & 1) ? (src >> 16) : (src & 0xffffu);
+            }
+            pair |= val << (16 * e);
+        }
+        w[q] = pair;
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// One segment's worth of outputs for one lane: tokens t0..t0+7 from the
+// 12-token window E (6 bf16x2 words, tokens t0-4 .. t0+7), scalar fp32 FMAs.
+template <int W, bool SILU>
+__device__ __forceinline__ uint4 cfa_outputs(const uint32_t (&E)[6], const float (&wt)[W], float bs) {
+    float u[12];
+#pragma unroll
+    for (int q = 0; q < 6; ++q) {
+        u[2 * q] = __uint_as_float(E[q] << 16);
+        u[2 * q + 1] = __uint_as_float(E[q] & 0xffff0000u);
+    }
+    uint32_t ow[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        float acc[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int i = 2 * p + e;  // output token t0 + i uses u[i+5-W .. i+4]
+            float s = fmaf(wt[0], u[i + 5 - W], bs);
+#pragma unroll
+            for (int k = 1; k < W; ++k) s = fmaf(wt[k], u[i + 5 - W + k], s);
+            acc[e] = s;
+        }
+        f32x2 r = pack2(acc[0], acc[1]);
+        if (SILU) r = silu2(r);
+        ow[p] = f32x2_to_bf16x2(r);
+    }
+    return make_uint4(ow[0], ow[1], ow[2], ow[3]);
+}
+
+template <int W, bool SILU>
+__global__ void __launch_bounds__(kCfaThreads, 4) fwd_cf_async_kernel(const FwdArgs a) {
+    extern __shared__ __align__(16) uint4 s_ring[];  // [kCfaSlots][kCfaThreads]
+    validate_sequence(a);
+    ChunkInfo ci;
+    if (!locate_chunk(a, kCfaChunk, blockIdx.x, ci)) return;
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int c = blockIdx.y * kCfaWarps + (tid >> 5);
+    if (c >= a.dim) return;  // warp-uniform
+
+    const uint16_t *const xc = a.x + c * a.xs_d;
+    const int cbeg = ci.start + ci.chunk * kCfaChunk;
+    const int cend = ci.start + min(ci.len, (ci.chunk + 1) * kCfaChunk);
+    const bool chunk0 = ci.chunk == 0;
+    const int lo = chunk0 ? cbeg : cbeg - (W - 1);
+    const int phase = static_cast<int>((reinterpret_cast<uintptr_t>(xc) >> 1) & 7u);
+    // first token of segment 0: aligned, at or before the first token needed
+    const int need0 = cbeg - (W - 1);
+    const int a0 = need0 - ((phase + need0) & 7);
+    const int nseg = (cend - a0 + 255) / 256;
+    // Segments [1, jin1) lie wholly inside [cbeg, cend) (segment 0 starts at
+    // a0 <= cbeg - (W-1), segment 1 at a0 + 256 > cbeg).
+    const int jin1 = max(1, (cend - a0) / 256);
+    uint4 *const ring_base = s_ring + tid;
+
+    // Start streaming the segments that lie wholly inside the chunk right
+    // away; segment 0 and the chunk's tail are assembled once the prior is
+    // known.  Segment j goes to slot j % kCfaSlots.
+#pragma unroll
+    for (int j = 1; j < kCfaSlots - 1; ++j) {
+        if (j < jin1) cp_async16(ring_base + j * kCfaThreads, xc + a0 + j * 256 + lane * 8);
+    }
+    int line;
+    if (!sequence_line(a, ci, line)) {
+        cp_async_commit();  // nothing may still land in this block's shared memory
+        cp_async_wait<0>();
+        return;
+    }
+    const bool init = chunk0 && a.st != nullptr && a.has_init != nullptr && a.has_init[ci.seq] != 0;
+    uint32_t prior01 = 0, prior23 = 0;  // prior columns 0..3, packed
+    if (init) {
+        const uint16_t *sp = a.st + line * a.ss_l + c * a.ss_d;
+        uint32_t p[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int j = 0; j < W - 1; ++j) p[j] = sp[j * a.ss_t];
+        prior01 = p[0] | (p[1] << 16);
+        prior23 = p[2] | (p[3] << 16);
+    }
+    auto issue_checked = [&](int seg) {
+        if (seg >= nseg) return;
+        const int t0 = a0 + seg * 256 + lane * 8;
+        uint4 *slot = ring_base + (seg % kCfaSlots) * kCfaThreads;
+        if (t0 >= lo && t0 + 8 <= cend) cp_async16(slot, xc + t0);
+        else *slot = cfa_edge_vector<W>(xc, t0, lo, cbeg, cend, chunk0, prior01, prior23);
+    };
+    // Segments 0..kCfaSlots-2 form one commit group each, in order.
+    issue_checked(0);
+    cp_async_commit();
+#pragma unroll
+    for (int j = 1; j < kCfaSlots - 1; ++j) {
+        if (j >= jin1) issue_checked(j);  // edge segments not started above
+        cp_async_commit();
+    }
+
+    float wt[W];
+#pragma unroll
+    for (int k = 0; k < W; ++k) wt[k] = bf16_bits(__ldg(a.w + c * a.ws_d + k * a.ws_k));
+    const float bs = a.bias ? bf16_bits(__ldg(a.bias + c)) : 0.0f;
+    uint32_t prev_z = 0, prev_w = 0;  // tokens before segment 0 are never needed
+    uint16_t *const oc = a.out + c * a.os_d;
+
+    auto window = [&](const uint4 &v, uint32_t (&E)[6]) {
+        const uint32_t up_z = __shfl_up_sync(kFullMask, v.z, 1);
+        const uint32_t up_w = __shfl_up_sync(kFullMask, v.w, 1);
+        const uint32_t pv_z = __shfl_sync(kFullMask, prev_z, 31);
+        const uint32_t pv_w = __shfl_sync(kFullMask, prev_w, 31);
+        prev_z = v.z;
+        prev_w = v.w;
+        E[0] = lane ? up_z : pv_z;
+        E[1] = lane ? up_w : pv_w;
+        E[2] = v.x;
+        E[3] = v.y;
+        E[4] = v.z;
+        E[5] = v.w;
+    };
+    auto step_checked = [&](int j) {
+        cp_async_wait<kCfaSlots - 2>();
+        const uint4 v = ring_base[(j % kCfaSlots) * kCfaThreads];
+        issue_checked(j + kCfaSlots - 1);
+        cp_async_commit();
+        uint32_t E[6];
+        window(v, E);
+        const int t0 = a0 + j * 256 + lane * 8;
+        if (t0 + 8 <= cbeg || t0 >= cend) return;
+        const uint4 o = cfa_outputs<W, SILU>(E, wt, bs);
+        if (t0 >= cbeg && t0 + 8 <= cend) {
+            __stcs(reinterpret_cast<uint4 *>(oc + t0), o);
+        } else {
+            const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int t = t0 + i;
+                if (t >= cbeg && t < cend)
+                    oc[t] = uint16_t((i & 1) ? (ow[i >> 1] >> 16) : (ow[i >> 1] & 0xffffu));
+            }
+        }
+    };
+
+    step_checked(0);
+    int j = 1;
+    // Lean steps: this segment and the one streamed in lie inside [cbeg, cend).
+    const uint16_t *nxt = xc + a0 + (j + kCfaSlots - 1) * 256 + lane * 8;
+    uint16_t *dst = oc + a0 + j * 256 + lane * 8;
+    for (; j + kCfaSlots - 1 < jin1; ++j) {
+        cp_async_wait<kCfaSlots - 2>();
+        const uint4 v = ring_base[(j % kCfaSlots) * kCfaThreads];
+        cp_async16(ring_base + ((j + kCfaSlots - 1) % kCfaSlots) * kCfaThreads, nxt);
+        cp_async_commit();
+        nxt += 256;
+        uint32_t E[6];
+        window(v, E);
+        __stcs(reinterpret_cast<uint4 *>(dst), cfa_outputs<W, SILU>(E, wt, bs));
+        dst += 256;
+    }
+    for (; j < nseg; ++j) step_checked(j);
+
+    if (chunk0 && a.st != nullptr) {
+        // New state = last W-1 entries of prior ++ x[sequence]; the prior was
+        // read by every lane above, before any lane writes the line.
+        uint16_t nb = 0;
+        if (lane < W - 1) {
+            const int idx = ci.len + lane;
+            if (idx < W - 1) {
+                const uint32_t src = idx < 2 ? prior01 : prior23;
+                nb = uint16_t((idx & 1) ? (src >> 16) : (src & 0xffffu));
+            } else {
+                nb = xc[ci.start + idx - (W - 1)];
+            }
+        }
+        __syncwarp();
+        if (lane < W - 1) a.st[line * a.ss_l + c * a.ss_d + lane * a.ss_t] = nb;
+    }
+}
+
 // ----------------------------------------------------------- dispatch ----
 
 using KernelFn = void (*)(FwdArgs);
@@ -441,6 +842,54 @@ KernelFn pick_kernel(int width, bool silu) {
     }
 #undef CCV_FWD_CASE
     return nullptr;
+}
+
+template <int W, bool SILU>
+int launch_cl_async_w(const FwdArgs &a, cudaStream_t stream) {
+    int dev = 0;
+    current_device_sms(&dev);
+    cudaError_t e;
+    if (resident_blocks<fwd_cl_async_kernel<W, SILU>>(kCaThreads, kCaSmem, dev, &e) == 0)
+        return static_cast<int>(e);
+    const dim3 grid(static_cast<unsigned>(a.total / kCaChunk + a.batch),
+                    static_cast<unsigned>((a.dim + kCaTileC - 1) / kCaTileC));
+    if (grid.y > 65535u) return CCV_ERR_SIZE;
+    fwd_cl_async_kernel<W, SILU><<<grid, kCaThreads, kCaSmem, stream>>>(a);
+    return launch_status();
+}
+
+template <int W, bool SILU>
+int launch_cf_async_w(const FwdArgs &a, cudaStream_t stream) {
+    int dev = 0;
+    current_device_sms(&dev);
+    cudaError_t e;
+    if (resident_blocks<fwd_cf_async_kernel<W, SILU>>(kCfaThreads, kCfaSmem, dev, &e) == 0)
+        return static_cast<int>(e);
+    const dim3 grid(static_cast<unsigned>(a.total / kCfaChunk + a.batch),
+                    static_cast<unsigned>((a.dim + kCfaWarps - 1) / kCfaWarps));
+    if (grid.y > 65535u) return CCV_ERR_SIZE;
+    fwd_cf_async_kernel<W, SILU><<<grid, kCfaThreads, kCfaSmem, stream>>>(a);
+    return launch_status();
+}
+
+int launch_cl_async(const FwdArgs &a, int width, bool silu, cudaStream_t stream) {
+    switch (width) {
+        case 2: return silu ? launch_cl_async_w<2, true>(a, stream) : launch_cl_async_w<2, false>(a, stream);
+        case 3: return silu ? launch_cl_async_w<3, true>(a, stream) : launch_cl_async_w<3, false>(a, stream);
+        case 4: return silu ? launch_cl_async_w<4, true>(a, stream) : launch_cl_async_w<4, false>(a, stream);
+        case 5: return silu ? launch_cl_async_w<5, true>(a, stream) : launch_cl_async_w<5, false>(a, stream);
+    }
+    return CCV_ERR_WIDTH;
+}
+
+int launch_cf_async(const FwdArgs &a, int width, bool silu, cudaStream_t stream) {
+    switch (width) {
+        case 2: return silu ? launch_cf_async_w<2, true>(a, stream) : launch_cf_async_w<2, false>(a, stream);
+        case 3: return silu ? launch_cf_async_w<3, true>(a, stream) : launch_cf_async_w<3, false>(a, stream);
+        case 4: return silu ? launch_cf_async_w<4, true>(a, stream) : launch_cf_async_w<4, false>(a, stream);
+        case 5: return silu ? launch_cf_async_w<5, true>(a, stream) : launch_cf_async_w<5, false>(a, stream);
+    }
+    return CCV_ERR_WIDTH;
 }
 
 }  // namespace
@@ -504,21 +953,21 @@ extern "C" int ccv_fwd(const void *x, int64_t x_stride_dim, int64_t x_stride_tok
     if (x_stride_dim == 1 && out_stride_dim == 1) {
         const bool vec = dim % 8 == 0 && aligned16(x) && aligned16(out) &&
                          x_stride_tok % 8 == 0 && out_stride_tok % 8 == 0;
-        const int vec_w = vec ? 8 : 1;
-        fn = vec ? pick_kernel<8, true>(width, is_silu) : pick_kernel<1, true>(width, is_silu);
         a.st_vec = vec && conv_states != nullptr && s_stride_dim == 1 && aligned16(conv_states) &&
                    s_stride_line % 8 == 0 && s_stride_tok % 8 == 0;
+        if (vec) return launch_cl_async(a, width, is_silu, stream);
+        fn = pick_kernel<1, true>(width, is_silu);
         grid = dim3(static_cast<unsigned>(total_tokens / kClChunk + batch),
-                    static_cast<unsigned>((dim + 32 * vec_w - 1) / (32 * vec_w)));
+                    static_cast<unsigned>((dim + 31) / 32));
     } else if (x_stride_tok == 1 && out_stride_tok == 1) {
         const uintptr_t xo = (reinterpret_cast<uintptr_t>(x) >> 1) & 7u;
         const uintptr_t oo = (reinterpret_cast<uintptr_t>(out) >> 1) & 7u;
-        const bool vec = (reinterpret_cast<uintptr_t>(x) & 1u) == 0 &&
-                         (reinterpret_cast<uintptr_t>(out) & 1u) == 0 && xo == oo &&
-                         (x_stride_dim - out_stride_dim) % 8 == 0;
-        const int seg = 32 * (vec ? 8 : 1);
-        fn = vec ? pick_kernel<8, false>(width, is_silu) : pick_kernel<1, false>(width, is_silu);
-        grid = dim3(static_cast<unsigned>(total_tokens / (kCfSegs * seg) + batch),
+        const bool same_phase = (reinterpret_cast<uintptr_t>(x) & 1u) == 0 &&
+                                (reinterpret_cast<uintptr_t>(out) & 1u) == 0 && xo == oo &&
+                                (x_stride_dim - out_stride_dim) % 8 == 0;
+        if (same_phase) return launch_cf_async(a, width, is_silu, stream);
+        fn = pick_kernel<1, false>(width, is_silu);
+        grid = dim3(static_cast<unsigned>(total_tokens / (kCfSegs * 32) + batch),
                     static_cast<unsigned>((dim + kWarps - 1) / kWarps));
     } else {
         fn = pick_kernel<1, true>(width, is_silu);

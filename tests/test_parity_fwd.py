@@ -98,6 +98,37 @@ def test_channel_first_unaligned_rows(extra):
     check(case)
 
 
+@pytest.mark.parametrize("shift", [1, 3])
+def test_channel_first_misaligned_base(shift):
+    """x and out start `shift` elements past a 16-byte boundary (same phase):
+    the channel-first kernel that needs only equal phases handles them."""
+    case = wl.varlen_prefill(551 + shift, [40, 2100, 5], 16, 4, num_cache_lines=3,
+                             layout="dim_tokens", has_init="all")
+    T = case.total_tokens
+
+    def shifted(src, device, fill=None):
+        buf = torch.zeros(case.dim * (T + 8) + 16, dtype=torch.bfloat16, device=device)
+        view = buf[shift:shift + case.dim * (T + 8)].view(case.dim, T + 8)[:, :T]
+        if fill is None:
+            view.copy_(src.to(device))
+        else:
+            view.view(torch.int16).fill_(fill)
+        return view
+
+    x_cpu, out_cpu = shifted(case.x, "cpu"), shifted(None, "cpu", -12345)
+    ref_states = case.conv_states.clone()
+    oracle.ccv_fwd(x_cpu, case.weight, case.bias, ref_states, case.query_start_loc,
+                   case.cache_indices, case.has_initial_state, case.activation, -1, out=out_cpu)
+    d = to_device(case.kwargs(), DEV)
+    d["x"] = shifted(case.x, DEV)
+    out = shifted(None, DEV, -12345)
+    assert d["x"].data_ptr() % 16 == 2 * shift and out.data_ptr() % 16 == 2 * shift
+    ccv.ccv_fwd(**d, out=out)
+    torch.cuda.synchronize()
+    assert_close(out, out_cpu, "misaligned out")
+    assert_bits(d["conv_states"], ref_states, "misaligned states")
+
+
 def test_mixed_layouts_use_generic_path():
     case = wl.varlen_prefill(601, [17, 140, 3], 24, 4, num_cache_lines=3, layout="tokens_dim",
                              has_init="bernoulli")
