@@ -344,7 +344,7 @@ def make_parts(dev, rank):
         meta(stream)
         conv(stream)
 
-    parts.append(Part("paged", "paged_kernel", 2, paged_bytes(c), c.T, paged_step))
+    parts.append(Part("paged", "paged_vec_kernel", 2, paged_bytes(c), c.T, paged_step))
     return parts, cases, dev_args
 
 

@@ -115,6 +115,67 @@ __device__ __forceinline__ int floor_div(int a, int b) {
     return (a % b != 0 && a < 0) ? q - 1 : q;
 }
 
+// The weights of 8 consecutive channels c0..c0+7 as tap-major bf16x2 words:
+// wpk[k] word q holds (w[c0+2q][k], w[c0+2q+1][k]).  When the weight matrix
+// is contiguous (dim, W) and 16-byte aligned, the thread's 8W values are W
+// 16-byte loads regrouped with one byte permute per word; otherwise they are
+// gathered one by one.  Channels at or beyond `dim` read as 0.
+template <int W>
+__device__ __forceinline__ void load_weights8(const uint16_t *w, int64_t ws_d, int64_t ws_k, int c0,
+                                              int dim, bool contiguous, uint4 (&wpk)[W]) {
+    uint32_t words[W][4];
+    if (contiguous && c0 + 8 <= dim) {
+        uint32_t raw[4 * W];  // elements c0*W .. c0*W + 8W - 1, two per word
+        const uint4 *src = reinterpret_cast<const uint4 *>(w + static_cast<int64_t>(c0) * W);
+#pragma unroll
+        for (int i = 0; i < W; ++i) {
+            const uint4 v = __ldg(src + i);
+            raw[4 * i] = v.x;
+            raw[4 * i + 1] = v.y;
+            raw[4 * i + 2] = v.z;
+            raw[4 * i + 3] = v.w;
+        }
+#pragma unroll
+        for (int k = 0; k < W; ++k)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int e1 = (2 * q) * W + k, e2 = (2 * q + 1) * W + k;
+                const uint32_t sel = ((e1 & 1) ? 0x32u : 0x10u) | ((e2 & 1) ? 0x7600u : 0x5400u);
+                words[k][q] = __byte_perm(raw[e1 >> 1], raw[e2 >> 1], sel);
+            }
+    } else {
+#pragma unroll
+        for (int k = 0; k < W; ++k)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int ca = c0 + 2 * q, cb = ca + 1;
+                const uint32_t lo = ca < dim ? __ldg(w + ca * ws_d + k * ws_k) : 0u;
+                const uint32_t hi = cb < dim ? __ldg(w + cb * ws_d + k * ws_k) : 0u;
+                words[k][q] = lo | (hi << 16);
+            }
+    }
+#pragma unroll
+    for (int k = 0; k < W; ++k) wpk[k] = make_uint4(words[k][0], words[k][1], words[k][2], words[k][3]);
+}
+
+// Bias of channels c0..c0+7 as fp32 (0 when absent or beyond dim).
+__device__ __forceinline__ void load_bias8(const uint16_t *bias, int c0, int dim, bool aligned,
+                                           float (&bs)[8]) {
+    if (bias == nullptr) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) bs[i] = 0.0f;
+        return;
+    }
+    if (aligned && c0 + 8 <= dim) {
+        Raw<8> r;
+        r.v = __ldg(reinterpret_cast<const uint4 *>(bias + c0));
+        r.to_float(bs);
+        return;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) bs[i] = c0 + i < dim ? bf16_bits(__ldg(bias + c0 + i)) : 0.0f;
+}
+
 // ------------------------------------------------------------ host side ----
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

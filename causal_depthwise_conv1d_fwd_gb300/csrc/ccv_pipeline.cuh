@@ -25,4 +25,21 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Wait until at most n of this thread's copy groups are pending (n <= 0:
+// all done; n >= 7: at most 7).  In a fully unrolled loop n folds to a
+// constant and only one wait instruction remains.
+__device__ __forceinline__ void cp_async_wait_upto(int n) {
+    switch (n) {
+        case 1: cp_async_wait<1>(); break;
+        case 2: cp_async_wait<2>(); break;
+        case 3: cp_async_wait<3>(); break;
+        case 4: cp_async_wait<4>(); break;
+        case 5: cp_async_wait<5>(); break;
+        case 6: cp_async_wait<6>(); break;
+        default:
+            if (n >= 7) cp_async_wait<7>();
+            else cp_async_wait<0>();
+    }
+}
+
 }  // namespace ccv

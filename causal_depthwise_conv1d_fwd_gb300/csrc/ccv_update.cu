@@ -6,18 +6,19 @@
 // the state left and append the new inputs, STEPS 3-5 bias, weights and the
 // token loop), non-speculative path.
 //
-// One thread owns 8 consecutive channels (16-byte vectors) of 4 consecutive
-// batch rows; the grid is ceil(batch / 4) x ceil(dim / 1024) blocks, fixed by
-// the sizes, so a CUDA graph replays it unchanged.  Every element of the state line and of out is
+// One thread owns 8 consecutive channels (16-byte vectors) of kRows
+// consecutive batch rows; the grid is ceil(batch / kRows) x ceil(dim / 1024)
+// blocks, fixed by the sizes, so a CUDA graph replays it unchanged.  Every element of the state line and of out is
 // read and written by the same thread, which makes the in-place state shift
 // and out == x (the page's wrapper writes the output over x) hazard-free.
 #include "ccv_common.cuh"
+#include "ccv_math2.cuh"
 
 namespace ccv {
 namespace {
 
 constexpr int kThreads = 128;
-constexpr int kRows = 4;  // batch rows per block
+constexpr int kRows = 2;  // batch rows per thread
 
 struct UpdArgs {
     const uint16_t *x;
@@ -35,6 +36,7 @@ struct UpdArgs {
     int *err;
     int ctiles;
     int x_vec, o_vec, st_vec;  // operand is addressable as 16-byte channel vectors
+    int w_vec, b_vec;          // weights contiguous (dim, W) / bias, 16-byte aligned
 };
 
 template <int VEC>
@@ -93,24 +95,50 @@ __device__ __forceinline__ void conv_token(const float (&wt)[W][VEC], const floa
     o.from_float(acc);
 }
 
-// A block covers kThreads*VEC channels of kRows consecutive batch rows, so the
-// weights it stages serve kRows rows.
+__device__ __forceinline__ uint32_t word_of(const uint4 &v, int q) {
+    return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
+}
+
+// Single-token decode for 8 channels of one row: taps over the raw state
+// window win[0..W-2] (oldest first) and x, native mixed-precision FMAs with
+// the bias entering through the first tap.
+template <int W, bool SILU>
+__device__ __forceinline__ uint4 decode_row(const uint4 (&wpk)[W], const float (&bs)[8],
+                                            const uint4 (&win)[W - 1], const uint4 &xv) {
+    float acc[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        fma_bf16x2_init(acc[2 * q], acc[2 * q + 1], word_of(win[0], q), word_of(wpk[0], q),
+                        bs[2 * q], bs[2 * q + 1]);
+#pragma unroll
+    for (int k = 1; k < W; ++k) {
+        const uint4 &u = k < W - 1 ? win[k < W - 1 ? k : 0] : xv;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) fma_bf16x2(acc[2 * q], acc[2 * q + 1], word_of(u, q), word_of(wpk[k], q));
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        f32x2 r = pack2(acc[2 * q], acc[2 * q + 1]);
+        if (SILU) r = silu2(r);
+        o[q] = f32x2_to_bf16x2(r);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// A block covers kThreads*VEC channels of kRows consecutive batch rows.  The
+// critical path is two dependent loads -- the rows' state-line indices, then
+// every row's state window and input at once -- with each thread's weights
+// loaded as 16-byte vectors while those loads are in flight.
 template <int W, bool SILU, int VEC>
-__global__ void __launch_bounds__(kThreads) update_kernel(const UpdArgs a) {
+__global__ void __launch_bounds__(kThreads, VEC == 8 ? 7 : 1) update_kernel(const UpdArgs a) {
     constexpr int TILE_C = kThreads * VEC;
     __shared__ __align__(16) uint16_t s_w[W * TILE_C];
     __shared__ __align__(16) uint16_t s_b[TILE_C];
     const int rg = blockIdx.x / a.ctiles;
     const int ct = blockIdx.x - rg * a.ctiles;
-    stage_weights<W>(a, ct * TILE_C, TILE_C, s_w, s_b);
     const int c0 = ct * TILE_C + threadIdx.x * VEC;
-    if (c0 >= a.dim) return;
-
-    float wt[W][VEC], bs[VEC];
-#pragma unroll
-    for (int k = 0; k < W; ++k)
-        reinterpret_cast<const Raw<VEC> *>(s_w + k * TILE_C)[threadIdx.x].to_float(wt[k]);
-    reinterpret_cast<const Raw<VEC> *>(s_b)[threadIdx.x].to_float(bs);
+    const bool active = c0 < a.dim;
 
     // Resolve the rows' state lines (skipped rows get line -1).
     int lines[kRows];
@@ -118,7 +146,7 @@ __global__ void __launch_bounds__(kThreads) update_kernel(const UpdArgs a) {
     for (int r = 0; r < kRows; ++r) {
         const int b = rg * kRows + r;
         int line = -1;
-        if (b < a.batch) {
+        if (active && b < a.batch) {
             line = a.idx ? __ldg(a.idx + b) : b;
             if (line == a.pad) {
                 line = -1;
@@ -130,38 +158,53 @@ __global__ void __launch_bounds__(kThreads) update_kernel(const UpdArgs a) {
         lines[r] = line;
     }
 
-    if (a.seqlen == 1) {
-        // Issue every row's window and input before any arithmetic.
-        Raw<VEC> win[kRows][W - 1], xv[kRows];
+    if (VEC == 8 && a.seqlen == 1) {
+        // Issue every row's window and input before anything else.
+        uint4 win[kRows][W - 1], xv[kRows];
 #pragma unroll
         for (int r = 0; r < kRows; ++r) {
             if (lines[r] < 0) continue;
             const uint16_t *sp = a.st + lines[r] * a.ss_l + c0 * a.ss_d;
 #pragma unroll
-            for (int j = 0; j < W - 1; ++j) win[r][j] = gather<VEC>(sp + j * a.ss_t, a.ss_d, a.st_vec);
+            for (int j = 0; j < W - 1; ++j) win[r][j] = gather<8>(sp + j * a.ss_t, a.ss_d, a.st_vec).v;
             const int b = rg * kRows + r;
-            xv[r] = gather<VEC>(a.x + b * a.xs_b + c0 * a.xs_d, a.xs_d, a.x_vec);
+            xv[r] = gather<8>(a.x + b * a.xs_b + c0 * a.xs_d, a.xs_d, a.x_vec).v;
         }
+        if (!active) return;
+        uint4 wpk[W];
+        load_weights8<W>(a.w, a.ws_d, a.ws_k, c0, a.dim, a.w_vec, wpk);
+        float bs[8];
+        load_bias8(a.bias, c0, a.dim, a.b_vec, bs);
 #pragma unroll
         for (int r = 0; r < kRows; ++r) {
             if (lines[r] < 0) continue;
             const int b = rg * kRows + r;
             uint16_t *sp = a.st + lines[r] * a.ss_l + c0 * a.ss_d;
-            float ring[W - 1][VEC], xf[VEC];
-#pragma unroll
-            for (int j = 0; j < W - 1; ++j) win[r][j].to_float(ring[j]);
-            xv[r].to_float(xf);
-            Raw<VEC> o;
-            conv_token<W, SILU, VEC>(wt, bs, ring, xf, o);
-            scatter<VEC>(a.out + b * a.os_b + c0 * a.os_d, a.os_d, a.o_vec, o);
+            Raw<8> o;
+            o.v = decode_row<W, SILU>(wpk, bs, win[r], xv[r]);
+            scatter<8>(a.out + b * a.os_b + c0 * a.os_d, a.os_d, a.o_vec, o);
             // The state keeps all but its oldest column and appends the input.
 #pragma unroll
-            for (int j = 0; j + 1 < W - 1; ++j) scatter<VEC>(sp + j * a.ss_t, a.ss_d, a.st_vec, win[r][j + 1]);
-            scatter<VEC>(sp + (W - 2) * a.ss_t, a.ss_d, a.st_vec, xv[r]);
+            for (int j = 0; j + 1 < W - 1; ++j) {
+                Raw<8> keep;
+                keep.v = win[r][j + 1];
+                scatter<8>(sp + j * a.ss_t, a.ss_d, a.st_vec, keep);
+            }
+            Raw<8> xin;
+            xin.v = xv[r];
+            scatter<8>(sp + (W - 2) * a.ss_t, a.ss_d, a.st_vec, xin);
         }
         return;
     }
 
+    // General path: any seqlen, scalar or vector channels, fp32 arithmetic.
+    stage_weights<W>(a, ct * TILE_C, TILE_C, s_w, s_b);
+    if (!active) return;
+    float wt[W][VEC], bs[VEC];
+#pragma unroll
+    for (int k = 0; k < W; ++k)
+        reinterpret_cast<const Raw<VEC> *>(s_w + k * TILE_C)[threadIdx.x].to_float(wt[k]);
+    reinterpret_cast<const Raw<VEC> *>(s_b)[threadIdx.x].to_float(bs);
     for (int r = 0; r < kRows; ++r) {
         if (lines[r] < 0) continue;
         const int b = rg * kRows + r;
@@ -272,6 +315,8 @@ extern "C" int ccv_update(const void *x, int64_t x_stride_b, int64_t x_stride_di
               (seqlen == 1 || out_stride_tok % 8 == 0);
     a.st_vec = vec && s_stride_dim == 1 && aligned16(conv_state) && s_stride_line % 8 == 0 &&
                s_stride_tok % 8 == 0;
+    a.w_vec = w_stride_w == 1 && w_stride_dim == width && aligned16(weight);
+    a.b_vec = bias != nullptr && aligned16(bias);
     a.ctiles = (dim + kThreads * vw - 1) / (kThreads * vw);
     const int64_t blocks = static_cast<int64_t>((batch + kRows - 1) / kRows) * a.ctiles;
     if (blocks > 0x7fffffffLL) return CCV_ERR_SIZE;

@@ -10,22 +10,25 @@
 // `_seq_metadata_kernel` (token -> request by binary search over
 // query_start_loc, padded rows zero).
 //
-// Layout of the work: a lane owns 8 consecutive channels (one 16-byte vector,
-// all in one head because ws is a multiple of 8) and walks a run of tokens;
-// the in-forward taps of a token are the x rows just before it, which the
-// thread already holds in registers, so x is read from memory once (plus a
-// W-1 row halo per run).  Only pre-forward taps touch the cache.  The grid
-// depends on T and C only, so CUDA graphs replay it unchanged.  Writes go to
-// this forward's slots and reads to earlier positions, which the caller keeps
-// disjoint, so one launch is race-free.
+// Layout of the work: in the vector kernel a lane owns 8 consecutive
+// channels (one 16-byte vector, all in one head because ws is a multiple of
+// 8) and a warp a run of 16 tokens; the scalar fallback has one channel per
+// lane and runs of 8.  One lane per token resolves the token's tap sources
+// once (shift/mask block arithmetic for power-of-two block sizes) and shares
+// them by shuffle.  In-forward taps are x rows; only pre-forward taps touch
+// the cache.  The grid depends on T and C only, so CUDA graphs replay it
+// unchanged.  Writes go to this forward's slots and reads to earlier
+// positions, which the caller keeps disjoint, so one launch is race-free.
 #include "ccv_common.cuh"
+#include "ccv_math2.cuh"
+#include "ccv_pipeline.cuh"
 
 namespace ccv {
 namespace {
 
 constexpr int kThreads = 128;
 constexpr int kWarps = kThreads / 32;
-constexpr int kRun = 16;  // tokens per warp (at most 32: one lane plans each)
+constexpr int kRun = 8;  // tokens per warp (at most 32: one lane plans each)
 constexpr int kBlockTokens = kWarps * kRun;
 
 struct PagedArgs {
@@ -46,8 +49,21 @@ struct PagedArgs {
     int bt_rows, max_blocks;
     const int32_t *qstart;
     int T, off_s, ws, C;
+    int n_shift;  // log2(N) when N is a power of two, else -1
+    int w_vec;    // weights contiguous [C, W] and 16-byte aligned
     int *err;
 };
+
+// (block, offset) of a non-negative flat position in blocks of N.
+__device__ __forceinline__ void split_pos(const PagedArgs &a, int64_t p, int64_t &blk, int64_t &off) {
+    if (a.n_shift >= 0) {
+        blk = p >> a.n_shift;
+        off = p & ((int64_t(1) << a.n_shift) - 1);
+    } else {
+        blk = p / a.N;
+        off = p - blk * a.N;
+    }
+}
 
 // Tap source kinds, two bits per tap in TokenPlan::kinds.
 constexpr int kTapZero = 0;    // PAD row or a position before 0: contributes nothing
@@ -64,23 +80,39 @@ struct TokenPlan {
     int64_t ins;
 };
 
+// The four per-token index values; a token past T reads as a PAD row.
+struct TokenMeta {
+    int64_t slot, pos;
+    int req, qs;
+};
+
+__device__ __forceinline__ TokenMeta load_meta(const PagedArgs &a, int t, bool valid) {
+    TokenMeta m{-1, 0, 0, 0};
+    if (valid) {
+        m.slot = __ldg(a.slot + t);
+        m.pos = __ldg(a.pos + t);
+        m.req = __ldg(a.seq_idx + t);
+        m.qs = __ldg(a.qstart + t);
+    }
+    return m;
+}
+
 // Lane l of a warp resolves the plan of token t (one lane per token), so the
 // per-token index loads and block-table lookups are issued once per warp and
 // overlap across the warp's tokens.
 template <int W>
-__device__ __forceinline__ TokenPlan<W> plan_token(const PagedArgs &a, int t) {
+__device__ __forceinline__ TokenPlan<W> plan_token(const PagedArgs &a, int t, const TokenMeta &m) {
     TokenPlan<W> p;
     p.kinds = 0;
     p.ins = -1;
 #pragma unroll
     for (int iw = 0; iw < W; ++iw) p.off[iw] = 0;
-    const int64_t slot = __ldg(a.slot + t);
+    const int64_t slot = m.slot, pos = m.pos;
+    const int req = m.req, qs = m.qs;
     if (slot < 0) return p;  // PAD row: every tap is zero, nothing is inserted
-    const int64_t pos = __ldg(a.pos + t);
-    const int req = __ldg(a.seq_idx + t);
-    const int qs = __ldg(a.qstart + t);
-    const int64_t blk = slot / a.N;
-    if (blk < a.num_blocks) p.ins = blk * a.cs_blk + (slot % a.N) * a.cs_n;
+    int64_t blk, boff;
+    split_pos(a, slot, blk, boff);
+    if (blk < a.num_blocks) p.ins = blk * a.cs_blk + boff * a.cs_n;
     else count_error(a.err);
 #pragma unroll
     for (int iw = 0; iw < W; ++iw) {
@@ -95,7 +127,8 @@ __device__ __forceinline__ TokenPlan<W> plan_token(const PagedArgs &a, int t) {
             p.kinds |= kTapX << (2 * iw);
             continue;
         }
-        int64_t lblk = src / a.N;
+        int64_t lblk, soff;
+        split_pos(a, src, lblk, soff);
         if (lblk > a.max_blocks - 1) lblk = a.max_blocks - 1;
         if (req < 0 || req >= a.bt_rows) {
             count_error(a.err);
@@ -107,7 +140,7 @@ __device__ __forceinline__ TokenPlan<W> plan_token(const PagedArgs &a, int t) {
             continue;
         }
         p.kinds |= kTapCache << (2 * iw);
-        p.off[iw] = pb * a.cs_blk + (src % a.N) * a.cs_n;
+        p.off[iw] = pb * a.cs_blk + soff * a.cs_n;
     }
     return p;
 }
@@ -118,138 +151,273 @@ __device__ __forceinline__ int64_t shfl64(int64_t v, int src) {
     return (static_cast<int64_t>(hi) << 32) | static_cast<uint32_t>(lo);
 }
 
-template <int W, bool SILU, bool RESID, int VEC>
-__global__ void __launch_bounds__(kThreads) paged_kernel(const PagedArgs a) {
-    constexpr int TILE_C = 32 * VEC;
-    constexpr int G = 8;  // x rows loaded together
-    __shared__ __align__(16) uint16_t s_w[W * TILE_C];
+// Fallback for unaligned or odd-width layouts: one channel per lane.
+template <int W, bool SILU, bool RESID>
+__global__ void __launch_bounds__(kThreads) paged_scalar_kernel(const PagedArgs a) {
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    const int cbase = blockIdx.y * TILE_C;
-    for (int i = threadIdx.x; i < W * TILE_C; i += kThreads) {
-        const int cl = i / W;
-        const int k = i - cl * W;
-        const int c = cbase + cl;
-        s_w[k * TILE_C + cl] = c < a.C ? __ldg(a.w + c * a.ws_c + k * a.ws_k) : uint16_t(0);
-    }
-    __syncthreads();
-
     const int t0 = blockIdx.x * kBlockTokens + warp * kRun;
     const int t1 = min(t0 + kRun, a.T);
     if (t0 >= t1) return;  // warp-uniform
-    const int c0 = cbase + lane * VEC;
+    const int c0 = blockIdx.y * 32 + lane;
     const bool active = c0 < a.C;  // inactive lanes still take part in the shuffles
 
-    float wt[W][VEC];
-#pragma unroll
-    for (int k = 0; k < W; ++k)
-        reinterpret_cast<const Raw<VEC> *>(s_w + k * TILE_C)[lane].to_float(wt[k]);
-
-    TokenPlan<W> mine;
-    mine.kinds = 0;
-    mine.ins = -1;
-#pragma unroll
-    for (int iw = 0; iw < W; ++iw) mine.off[iw] = 0;
-    if (t0 + lane < t1) mine = plan_token<W>(a, t0 + lane);
-
-    const int head = active ? c0 / a.ws : 0;
-    const int64_t chan_off = static_cast<int64_t>(head) * a.cs_h + a.off_s + (active ? c0 % a.ws : 0);
-
-    // ring[m] holds x row (t - (W-1) + m) for the token t being processed.
-    float ring[W - 1][VEC];
+    float ring[W - 1];
 #pragma unroll
     for (int m = 0; m < W - 1; ++m) {
         const int row = t0 - (W - 1) + m;
-        if (active && row >= 0) load_plain<VEC>(a.x + row * a.xs_t + c0).to_float(ring[m]);
-        else
+        ring[m] = active && row >= 0 ? bf16_bits(a.x[row * a.xs_t + c0]) : 0.0f;
+    }
+    uint16_t xg[kRun];
 #pragma unroll
-            for (int v = 0; v < VEC; ++v) ring[m][v] = 0.0f;
+    for (int u = 0; u < kRun; ++u) xg[u] = active && t0 + u < t1 ? __ldg(a.x + (t0 + u) * a.xs_t + c0) : 0;
+
+    const TokenPlan<W> mine = plan_token<W>(a, t0 + lane, load_meta(a, t0 + lane, t0 + lane < t1));
+
+    const int head = active ? c0 / a.ws : 0;
+    const int64_t chan_off = static_cast<int64_t>(head) * a.cs_h + a.off_s + (active ? c0 % a.ws : 0);
+    float wt[W];
+#pragma unroll
+    for (int k = 0; k < W; ++k) wt[k] = active ? bf16_bits(__ldg(a.w + c0 * a.ws_c + k * a.ws_k)) : 0.0f;
+
+#pragma unroll
+    for (int u = 0; u < kRun; ++u) {
+        const int t = t0 + u;
+        if (t >= t1) break;  // warp-uniform
+        const int kinds = __shfl_sync(kFullMask, mine.kinds, u);
+        int64_t off[W];
+#pragma unroll
+        for (int iw = 0; iw < W; ++iw) off[iw] = shfl64(mine.off[iw], u);
+        const int64_t ins = shfl64(mine.ins, u);
+        const float xf = bf16_bits(xg[u]);
+        if (active && ins >= 0) a.cache[ins + chan_off] = xg[u];
+        float acc = 0.0f;
+#pragma unroll
+        for (int iw = 0; iw < W; ++iw) {
+            const int kind = (kinds >> (2 * iw)) & 3;
+            if (kind == kTapZero) continue;
+            const float tap = kind == kTapX ? (iw == W - 1 ? xf : ring[iw < W - 1 ? iw : 0])
+                                            : bf16_bits(a.cache[off[iw] + chan_off]);
+            acc = fmaf(tap, wt[iw], acc);
+        }
+        if (SILU) acc = silu(acc);
+        if (RESID) acc = acc + xf;
+        if (active) a.out[t * a.os_t + c0] = round_bf16(acc);
+#pragma unroll
+        for (int m = 0; m < W - 2; ++m) ring[m] = ring[m + 1];
+        ring[W - 2] = xf;
+    }
+}
+
+// Vector kernel: a lane owns 8 channels (16 bytes) and a warp a run of
+// kVecRun tokens.  The warp stages its x rows (the W-1 before the run, then
+// the run) in shared memory with per-lane asynchronous copies; each lane
+// reads back only the slots it filled, so its own wait is the only
+// synchronisation.  When every token of the run takes all W taps from x (an
+// interior stretch of a prefill, the usual case), a straight loop keeps the
+// taps in a register ring of fp32 pairs and shuffles only the insert offset;
+// otherwise each token follows its plan (x rows from shared memory, cache
+// taps from global memory).
+constexpr int kVecRun = 16;
+constexpr int kStageGroup = 4;  // staged rows per asynchronous-copy group
+constexpr int kVecBlockTokens = kWarps * kVecRun;
+constexpr int kVecChannels = 32 * 8;
+
+template <int W>
+constexpr int vec_smem_bytes() {
+    return kWarps * (kVecRun + W - 1) * 32 * 16;
+}
+
+template <int W>
+constexpr int all_x_kinds() {
+    int k = 0;
+    for (int iw = 0; iw < W; ++iw) k |= kTapX << (2 * iw);
+    return k;
+}
+
+__device__ __forceinline__ void widen8(const uint4 &v, f32x2 (&f)[4]) {
+    f[0] = widen2(v.x);
+    f[1] = widen2(v.y);
+    f[2] = widen2(v.z);
+    f[3] = widen2(v.w);
+}
+
+// SiLU, then the residual, then bf16 rounding of one lane's 8 outputs.
+template <bool SILU, bool RESID>
+__device__ __forceinline__ uint4 finish8(const f32x2 (&acc)[4], const f32x2 (&xf)[4]) {
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        f32x2 r = acc[q];
+        if (SILU) r = silu2(r);
+        if (RESID) r = add2(r, xf[q]);
+        o[q] = f32x2_to_bf16x2(r);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+template <int W, bool SILU, bool RESID>
+__global__ void __launch_bounds__(kThreads, 4) paged_vec_kernel(const PagedArgs a) {
+    extern __shared__ uint4 stage[];
+    constexpr int R = kVecRun + W - 1;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int t0 = blockIdx.x * kVecBlockTokens + warp * kVecRun;
+    const int t1 = min(t0 + kVecRun, a.T);
+    if (t0 >= t1) return;  // warp-uniform
+    const int c0 = blockIdx.y * kVecChannels + lane * 8;
+    const bool active = c0 < a.C;  // inactive lanes still take part in the shuffles
+    uint4 *xs = stage + warp * R * 32 + lane;  // row m of the warp's window at xs[m * 32]
+
+    // Every load that does not depend on another goes out first -- weights,
+    // the lane's token indices, then the staged x rows -- so a warp waits for
+    // one memory round trip before the block-table lookups, not three.
+    uint4 wpk[W];
+    load_weights8<W>(a.w, a.ws_c, a.ws_k, active ? c0 : 0, a.C, a.w_vec, wpk);
+    const TokenMeta meta = load_meta(a, t0 + lane, t0 + lane < t1);
+#pragma unroll
+    for (int m = 0; m < R; ++m) {
+        const int row = t0 - (W - 1) + m;
+        if (active && row >= 0 && row < t1) cp_async16(xs + m * 32, a.x + row * a.xs_t + c0);
+        else xs[m * 32] = make_uint4(0u, 0u, 0u, 0u);
+        if (m % kStageGroup == kStageGroup - 1 || m == R - 1) cp_async_commit();
     }
 
-    for (int g = t0; g < t1; g += G) {
-        Raw<VEC> xg[G];
+    const TokenPlan<W> mine = plan_token<W>(a, t0 + lane, meta);
+    const bool all_x = __all_sync(kFullMask, t0 + lane >= t1 ||
+                                                 (mine.kinds == all_x_kinds<W>() && mine.ins >= 0));
+
+    const int head = active ? c0 / a.ws : 0;
+    const int64_t chan_off = static_cast<int64_t>(head) * a.cs_h + a.off_s + (active ? c0 % a.ws : 0);
+    f32x2 wf[W][4];
 #pragma unroll
-        for (int u = 0; u < G; ++u) {
-            if (active && g + u < t1) xg[u] = load_stream<VEC>(a.x + (g + u) * a.xs_t + c0);
-            else xg[u].zero();
+    for (int k = 0; k < W; ++k) widen8(wpk[k], wf[k]);
+    const int n = t1 - t0;
+
+    if (all_x) {
+        // Token u needs staged rows up to u + W - 1: wait only for the copy
+        // groups up to that row, so stores start while later rows arrive.
+        constexpr int kGroups = (R + kStageGroup - 1) / kStageGroup;
+        f32x2 ring[W - 1][4];
+        cp_async_wait<kGroups - 1 - (W - 1) / kStageGroup>();  // rows 0 .. W-1
+#pragma unroll
+        for (int m = 0; m < W - 1; ++m) widen8(xs[m * 32], ring[m]);
+#pragma unroll
+        for (int u = 0; u < kVecRun; ++u) {
+            if (u >= n) break;  // warp-uniform
+            // Wait only where the needed group changes: a wait orders all
+            // memory accesses around it, so tokens between two waits can
+            // still be interleaved by the compiler.
+            const int need = (u + W - 1) / kStageGroup;
+            if (u > 0 && need != (u + W - 2) / kStageGroup) cp_async_wait_upto(kGroups - 1 - need);
+            const int64_t ins = shfl64(mine.ins, u);
+            const uint4 xr = xs[(u + W - 1) * 32];
+            if (active) *reinterpret_cast<uint4 *>(a.cache + ins + chan_off) = xr;
+            f32x2 xf[4];
+            widen8(xr, xf);
+            f32x2 acc[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                acc[q] = fma2(ring[0][q], wf[0][q], 0ull);
+#pragma unroll
+                for (int iw = 1; iw < W - 1; ++iw) acc[q] = fma2(ring[iw][q], wf[iw][q], acc[q]);
+                acc[q] = fma2(xf[q], wf[W - 1][q], acc[q]);
+            }
+            const uint4 o = finish8<SILU, RESID>(acc, xf);
+            if (active) __stcs(reinterpret_cast<uint4 *>(a.out + (t0 + u) * a.os_t + c0), o);
+#pragma unroll
+            for (int m = 0; m < W - 2; ++m)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) ring[m][q] = ring[m + 1][q];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) ring[W - 2][q] = xf[q];
+        }
+        return;
+    }
+
+    // General path.  The cache taps of a group of tokens are loaded before
+    // any of the group's stores, so their latencies overlap instead of
+    // queueing behind the stores (which the compiler cannot prove disjoint).
+    constexpr int kGroup = W <= 4 ? 12 / (W - 1) : 2;  // 48 or 32 registers of taps
+    cp_async_wait<0>();
+#pragma unroll 1
+    for (int g = 0; g < n; g += kGroup) {
+        uint4 cached[kGroup][W - 1];
+#pragma unroll
+        for (int j = 0; j < kGroup; ++j) {
+            // g + j < 16 + 12 <= 32; lanes without a token carry an empty plan.
+            const int kinds = __shfl_sync(kFullMask, mine.kinds, g + j);
+#pragma unroll
+            for (int iw = 0; iw < W - 1; ++iw) {
+                const int64_t off = shfl64(mine.off[iw], g + j);
+                cached[j][iw] = make_uint4(0u, 0u, 0u, 0u);
+                if (active && ((kinds >> (2 * iw)) & 3) == kTapCache)
+                    cached[j][iw] = *reinterpret_cast<const uint4 *>(a.cache + off + chan_off);
+            }
         }
 #pragma unroll
-        for (int u = 0; u < G; ++u) {
-            const int t = g + u;
-            if (t >= t1) break;  // warp-uniform
-            const int src_lane = t - t0;
-            const int kinds = __shfl_sync(kFullMask, mine.kinds, src_lane);
-            int64_t off[W];
-#pragma unroll
-            for (int iw = 0; iw < W; ++iw) off[iw] = shfl64(mine.off[iw], src_lane);
-            const int64_t ins = shfl64(mine.ins, src_lane);
-
-            float xf[VEC];
-            xg[u].to_float(xf);
-            if (active && ins >= 0) store_plain<VEC>(a.cache + ins + chan_off, xg[u]);
-
-            Raw<VEC> cached[W];
-#pragma unroll
-            for (int iw = 0; iw < W; ++iw) {
-                if (active && ((kinds >> (2 * iw)) & 3) == kTapCache)
-                    cached[iw] = load_plain<VEC>(a.cache + off[iw] + chan_off);
-                else
-                    cached[iw].zero();
-            }
-            float acc[VEC];
-#pragma unroll
-            for (int v = 0; v < VEC; ++v) acc[v] = 0.0f;
+        for (int j = 0; j < kGroup; ++j) {
+            const int u = g + j;
+            if (u >= n) break;  // warp-uniform
+            const int kinds = __shfl_sync(kFullMask, mine.kinds, u);
+            const int64_t ins = shfl64(mine.ins, u);
+            const int64_t off_last = shfl64(mine.off[W - 1], u);
+            const uint4 xr = xs[(u + W - 1) * 32];
+            if (active && ins >= 0) *reinterpret_cast<uint4 *>(a.cache + ins + chan_off) = xr;
+            f32x2 acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
             for (int iw = 0; iw < W; ++iw) {
                 const int kind = (kinds >> (2 * iw)) & 3;
                 if (kind == kTapZero) continue;
-                float tap[VEC];
-                if (kind == kTapX) {
+                uint4 tap = make_uint4(0u, 0u, 0u, 0u);
+                if (kind == kTapX) tap = xs[(u + iw) * 32];
+                else if (iw < W - 1) tap = cached[j][iw < W - 1 ? iw : 0];
+                // The token's own position comes from the cache only when its
+                // query start lies after it (inconsistent metadata).
+                else if (active) tap = *reinterpret_cast<const uint4 *>(a.cache + off_last + chan_off);
+                f32x2 tf[4];
+                widen8(tap, tf);
 #pragma unroll
-                    for (int v = 0; v < VEC; ++v) tap[v] = iw == W - 1 ? xf[v] : ring[iw][v];
-                } else {
-                    cached[iw].to_float(tap);
-                }
-#pragma unroll
-                for (int v = 0; v < VEC; ++v) acc[v] = fmaf(tap[v], wt[iw][v], acc[v]);
+                for (int q = 0; q < 4; ++q) acc[q] = fma2(tf[q], wf[iw][q], acc[q]);
             }
-#pragma unroll
-            for (int v = 0; v < VEC; ++v) {
-                if (SILU) acc[v] = silu(acc[v]);
-                if (RESID) acc[v] = acc[v] + xf[v];
-            }
-            if (active) {
-                Raw<VEC> o;
-                o.from_float(acc);
-                store_stream<VEC>(a.out + t * a.os_t + c0, o);
-            }
-#pragma unroll
-            for (int m = 0; m < W - 2; ++m)
-#pragma unroll
-                for (int v = 0; v < VEC; ++v) ring[m][v] = ring[m + 1][v];
-#pragma unroll
-            for (int v = 0; v < VEC; ++v) ring[W - 2][v] = xf[v];
+            f32x2 xf[4];
+            widen8(xr, xf);
+            const uint4 o = finish8<SILU, RESID>(acc, xf);
+            if (active) __stcs(reinterpret_cast<uint4 *>(a.out + (t0 + u) * a.os_t + c0), o);
         }
     }
 }
 
 using PagedFn = void (*)(PagedArgs);
 
-template <int VEC, int W>
-PagedFn pick_w(bool silu, bool resid) {
-    if (silu) return resid ? paged_kernel<W, true, true, VEC> : paged_kernel<W, true, false, VEC>;
-    return resid ? paged_kernel<W, false, true, VEC> : paged_kernel<W, false, false, VEC>;
+template <int W>
+PagedFn pick_w(bool vec, bool silu, bool resid) {
+    if (vec) {
+        if (silu) return resid ? paged_vec_kernel<W, true, true> : paged_vec_kernel<W, true, false>;
+        return resid ? paged_vec_kernel<W, false, true> : paged_vec_kernel<W, false, false>;
+    }
+    if (silu) return resid ? paged_scalar_kernel<W, true, true> : paged_scalar_kernel<W, true, false>;
+    return resid ? paged_scalar_kernel<W, false, true> : paged_scalar_kernel<W, false, false>;
 }
 
-template <int VEC>
-PagedFn pick_kernel(int width, bool silu, bool resid) {
+PagedFn pick_kernel(int width, bool vec, bool silu, bool resid) {
     switch (width) {
-        case 2: return pick_w<VEC, 2>(silu, resid);
-        case 3: return pick_w<VEC, 3>(silu, resid);
-        case 4: return pick_w<VEC, 4>(silu, resid);
-        case 5: return pick_w<VEC, 5>(silu, resid);
+        case 2: return pick_w<2>(vec, silu, resid);
+        case 3: return pick_w<3>(vec, silu, resid);
+        case 4: return pick_w<4>(vec, silu, resid);
+        case 5: return pick_w<5>(vec, silu, resid);
     }
     return nullptr;
+}
+
+int vec_smem(int width) {
+    switch (width) {
+        case 2: return vec_smem_bytes<2>();
+        case 3: return vec_smem_bytes<3>();
+        case 4: return vec_smem_bytes<4>();
+        case 5: return vec_smem_bytes<5>();
+    }
+    return 0;
 }
 
 constexpr int kMetaThreads = 256;
@@ -358,17 +526,19 @@ extern "C" int paged_sconv_fwd(const void *x, int64_t x_stride_t, void *cache,
     a.off_s = off_s;
     a.ws = ws;
     a.C = C;
+    a.n_shift = (N & (N - 1)) == 0 ? __builtin_ctz(static_cast<unsigned>(N)) : -1;
+    a.w_vec = w_stride_w == 1 && w_stride_c == width && aligned16(weight);
     a.err = err_count;
 
     const bool vec = ws % 8 == 0 && off_s % 8 == 0 && aligned16(x) && aligned16(out) &&
                      aligned16(cache) && x_stride_t % 8 == 0 && out_stride_t % 8 == 0 &&
                      c_stride_blk % 8 == 0 && c_stride_h % 8 == 0 && c_stride_n % 8 == 0;
-    const int vw = vec ? 8 : 1;
-    PagedFn fn = vec ? pick_kernel<8>(width, silu != 0, residual != 0)
-                     : pick_kernel<1>(width, silu != 0, residual != 0);
-    const dim3 grid(static_cast<unsigned>((T + kBlockTokens - 1) / kBlockTokens),
-                    static_cast<unsigned>((C + 32 * vw - 1) / (32 * vw)));
+    PagedFn fn = pick_kernel(width, vec, silu != 0, residual != 0);
+    const int block_tokens = vec ? kVecBlockTokens : kBlockTokens;
+    const int tile_c = vec ? kVecChannels : 32;
+    const dim3 grid(static_cast<unsigned>((T + block_tokens - 1) / block_tokens),
+                    static_cast<unsigned>((C + tile_c - 1) / tile_c));
     if (grid.y > 65535u) return CCV_ERR_SIZE;
-    fn<<<grid, kThreads, 0, stream>>>(a);
+    fn<<<grid, kThreads, vec ? vec_smem(width) : 0, stream>>>(a);
     return launch_status();
 }
