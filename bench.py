@@ -251,13 +251,29 @@ def whole_job_rate(units_per_rank_step: float, steps: int, world: int, max_secon
 
 # ------------------------------------------------------------- roofline ----
 
-def kernel_sources_sha() -> str:
+# Translation unit that defines each kernel the bench times.
+KERNEL_SOURCE = {
+    "fwd_cl_async_kernel": "ccv_fwd.cu",
+    "fwd_cf_async_kernel": "ccv_fwd.cu",
+    "update_kernel": "ccv_update.cu",
+    "paged_vec_kernel": "paged_sconv.cu",
+    "seq_metadata_kernel": "paged_sconv.cu",
+}
+
+
+def kernel_sources_sha(kernel: str) -> str:
+    """Hash of the sources `kernel` is built from: its own .cu file, the
+    shared device headers and the C header."""
     from causal_depthwise_conv1d_fwd_gb300 import build as lib_build
 
+    own = KERNEL_SOURCE[kernel]
     h = hashlib.sha256()
     for f in sorted(lib_build._inputs()):
+        name = os.path.basename(f)
+        if f.endswith(".cu") and name != own:
+            continue
         with open(f, "rb") as fh:
-            h.update(os.path.basename(f).encode())
+            h.update(name.encode())
             h.update(fh.read())
     return h.hexdigest()[:16]
 
@@ -268,7 +284,9 @@ def recorded_traffic(kernel: str):
     pdir = os.path.join(ROOT, "profiles")
     if not os.path.isdir(pdir):
         return None
-    sha = kernel_sources_sha()
+    if kernel not in KERNEL_SOURCE:
+        return None
+    sha = kernel_sources_sha(kernel)
     pat = re.compile(r"bench-traffic:\s*kernel=(\S+)\s+bytes_per_launch=(\d+)\s+"
                      r"source_sha=([0-9a-f]+)")
     for f in sorted(os.listdir(pdir)):
