@@ -651,28 +651,25 @@ __device__ __noinline__ uint4 cfa_edge_vector(const uint16_t *xc, int t0, int lo
 }
 
 // One segment's worth of outputs for one lane: tokens t0..t0+7 from the
-// 12-token window E (6 bf16x2 words, tokens t0-4 .. t0+7), scalar fp32 FMAs.
+// 12-token window E (6 bf16x2 words, tokens t0-4 .. t0+7).  Output pair p
+// (tokens 2p, 2p+1) takes tap k from window tokens i0 = 2p+5-W+k and i0+1:
+// one word of E when i0 is even, else the two halves that straddle a word
+// boundary; native bf16 x bf16 + fp32 FMAs with the weight broadcast to both
+// halves (bias first, then taps 0..W-1, one rounding each).
 template <int W, bool SILU>
-__device__ __forceinline__ uint4 cfa_outputs(const uint32_t (&E)[6], const float (&wt)[W], float bs) {
-    float u[12];
-#pragma unroll
-    for (int q = 0; q < 6; ++q) {
-        u[2 * q] = __uint_as_float(E[q] << 16);
-        u[2 * q + 1] = __uint_as_float(E[q] & 0xffff0000u);
-    }
+__device__ __forceinline__ uint4 cfa_outputs(const uint32_t (&E)[6], const uint32_t (&wb)[W], float bs) {
     uint32_t ow[4];
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
-        float acc[2];
+        float lo, hi;
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int i = 2 * p + e;  // output token t0 + i uses u[i+5-W .. i+4]
-            float s = fmaf(wt[0], u[i + 5 - W], bs);
-#pragma unroll
-            for (int k = 1; k < W; ++k) s = fmaf(wt[k], u[i + 5 - W + k], s);
-            acc[e] = s;
+        for (int k = 0; k < W; ++k) {
+            const int i0 = 2 * p + 5 - W + k;
+            const uint32_t xw = (i0 & 1) ? __byte_perm(E[i0 >> 1], E[(i0 >> 1) + 1], 0x5432) : E[i0 >> 1];
+            if (k == 0) fma_bf16x2_init(lo, hi, xw, wb[0], bs, bs);
+            else fma_bf16x2(lo, hi, xw, wb[k]);
         }
-        f32x2 r = pack2(acc[0], acc[1]);
+        f32x2 r = pack2(lo, hi);
         if (SILU) r = silu2(r);
         ow[p] = f32x2_to_bf16x2(r);
     }
@@ -744,9 +741,9 @@ __global__ void __launch_bounds__(kCfaThreads, 4) fwd_cf_async_kernel(const FwdA
         cp_async_commit();
     }
 
-    float wt[W];
+    uint32_t wt[W];  // tap k's bf16 weight in both halves
 #pragma unroll
-    for (int k = 0; k < W; ++k) wt[k] = bf16_bits(__ldg(a.w + c * a.ws_d + k * a.ws_k));
+    for (int k = 0; k < W; ++k) wt[k] = 0x10001u * __ldg(a.w + c * a.ws_d + k * a.ws_k);
     const float bs = a.bias ? bf16_bits(__ldg(a.bias + c)) : 0.0f;
     uint32_t prev_z = 0, prev_w = 0;  // tokens before segment 0 are never needed
     uint16_t *const oc = a.out + c * a.os_d;
@@ -793,6 +790,23 @@ __global__ void __launch_bounds__(kCfaThreads, 4) fwd_cf_async_kernel(const FwdA
     // Lean steps: this segment and the one streamed in lie inside [cbeg, cend).
     const uint16_t *nxt = xc + a0 + (j + kCfaSlots - 1) * 256 + lane * 8;
     uint16_t *dst = oc + a0 + j * 256 + lane * 8;
+    // Groups of kCfaSlots lean steps starting at j = 1 (mod kCfaSlots):
+    // segment j+u sits in slot (1+u) % kCfaSlots and the segment streamed
+    // in goes to slot u, so every slot offset is a constant.
+    for (; j + 2 * kCfaSlots - 2 < jin1; j += kCfaSlots) {
+#pragma unroll
+        for (int u = 0; u < kCfaSlots; ++u) {
+            cp_async_wait<kCfaSlots - 2>();
+            const uint4 v = ring_base[((1 + u) % kCfaSlots) * kCfaThreads];
+            cp_async16(ring_base + u * kCfaThreads, nxt + u * 256);
+            cp_async_commit();
+            uint32_t E[6];
+            window(v, E);
+            __stcs(reinterpret_cast<uint4 *>(dst + u * 256), cfa_outputs<W, SILU>(E, wt, bs));
+        }
+        nxt += kCfaSlots * 256;
+        dst += kCfaSlots * 256;
+    }
     for (; j + kCfaSlots - 1 < jin1; ++j) {
         cp_async_wait<kCfaSlots - 2>();
         const uint4 v = ring_base[(j % kCfaSlots) * kCfaThreads];

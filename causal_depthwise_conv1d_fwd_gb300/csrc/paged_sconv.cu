@@ -12,7 +12,7 @@
 //
 // Layout of the work: in the vector kernel a lane owns 8 consecutive
 // channels (one 16-byte vector, all in one head because ws is a multiple of
-// 8) and a warp a run of 16 tokens; the scalar fallback has one channel per
+// 8) and a warp a run of 8 tokens; the scalar fallback has one channel per
 // lane and runs of 8.  One lane per token resolves the token's tap sources
 // once (shift/mask block arithmetic for power-of-two block sizes) and shares
 // them by shuffle.  In-forward taps are x rows; only pre-forward taps touch
@@ -215,10 +215,13 @@ __global__ void __launch_bounds__(kThreads) paged_scalar_kernel(const PagedArgs 
 // reads back only the slots it filled, so its own wait is the only
 // synchronisation.  When every token of the run takes all W taps from x (an
 // interior stretch of a prefill, the usual case), a straight loop keeps the
-// taps in a register ring of fp32 pairs and shuffles only the insert offset;
-// otherwise each token follows its plan (x rows from shared memory, cache
-// taps from global memory).
-constexpr int kVecRun = 16;
+// taps in a register ring of raw bf16 rows and shuffles only the insert
+// offset; otherwise each token follows its plan (x rows from shared memory,
+// cache taps from global memory).  Taps are native bf16 x bf16 + fp32 FMAs
+// on packed weights.  Short runs and a register bound of 7 blocks per SM
+// keep enough warps in flight: the work is latency-bound, not
+// bandwidth-bound, at serving batch sizes.
+constexpr int kVecRun = 8;
 constexpr int kStageGroup = 4;  // staged rows per asynchronous-copy group
 constexpr int kVecBlockTokens = kWarps * kVecRun;
 constexpr int kVecChannels = 32 * 8;
@@ -235,29 +238,45 @@ constexpr int all_x_kinds() {
     return k;
 }
 
-__device__ __forceinline__ void widen8(const uint4 &v, f32x2 (&f)[4]) {
-    f[0] = widen2(v.x);
-    f[1] = widen2(v.y);
-    f[2] = widen2(v.z);
-    f[3] = widen2(v.w);
+__device__ __forceinline__ uint32_t word_of(const uint4 &v, int q) {
+    return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
 }
 
-// SiLU, then the residual, then bf16 rounding of one lane's 8 outputs.
+// SiLU, then the residual (x of the token, widened exactly), then bf16
+// rounding of one lane's 8 outputs.
 template <bool SILU, bool RESID>
-__device__ __forceinline__ uint4 finish8(const f32x2 (&acc)[4], const f32x2 (&xf)[4]) {
+__device__ __forceinline__ uint4 finish_row(const float (&acc)[8], const uint4 &xr) {
     uint32_t o[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        f32x2 r = acc[q];
+        f32x2 r = pack2(acc[2 * q], acc[2 * q + 1]);
         if (SILU) r = silu2(r);
-        if (RESID) r = add2(r, xf[q]);
+        if (RESID) r = add2(r, widen2(word_of(xr, q)));
         o[q] = f32x2_to_bf16x2(r);
     }
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// One token whose W taps all come from x: ring[0..W-2] (oldest first) and
+// xr, native bf16 x bf16 + fp32 FMAs from zero (no bias), taps in order.
 template <int W, bool SILU, bool RESID>
-__global__ void __launch_bounds__(kThreads, 4) paged_vec_kernel(const PagedArgs a) {
+__device__ __forceinline__ uint4 paged_row(const uint4 (&wpk)[W], const uint4 (&ring)[W - 1],
+                                           const uint4 &xr) {
+    float acc[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        fma_bf16x2_init(acc[2 * q], acc[2 * q + 1], word_of(ring[0], q), word_of(wpk[0], q), 0.0f, 0.0f);
+#pragma unroll
+    for (int k = 1; k < W; ++k) {
+        const uint4 &u = k < W - 1 ? ring[k < W - 1 ? k : 0] : xr;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) fma_bf16x2(acc[2 * q], acc[2 * q + 1], word_of(u, q), word_of(wpk[k], q));
+    }
+    return finish_row<SILU, RESID>(acc, xr);
+}
+
+template <int W, bool SILU, bool RESID>
+__global__ void __launch_bounds__(kThreads, 7) paged_vec_kernel(const PagedArgs a) {
     extern __shared__ uint4 stage[];
     constexpr int R = kVecRun + W - 1;
     const int lane = threadIdx.x & 31;
@@ -289,19 +308,16 @@ __global__ void __launch_bounds__(kThreads, 4) paged_vec_kernel(const PagedArgs 
 
     const int head = active ? c0 / a.ws : 0;
     const int64_t chan_off = static_cast<int64_t>(head) * a.cs_h + a.off_s + (active ? c0 % a.ws : 0);
-    f32x2 wf[W][4];
-#pragma unroll
-    for (int k = 0; k < W; ++k) widen8(wpk[k], wf[k]);
     const int n = t1 - t0;
 
     if (all_x) {
         // Token u needs staged rows up to u + W - 1: wait only for the copy
         // groups up to that row, so stores start while later rows arrive.
         constexpr int kGroups = (R + kStageGroup - 1) / kStageGroup;
-        f32x2 ring[W - 1][4];
+        uint4 ring[W - 1];
         cp_async_wait<kGroups - 1 - (W - 1) / kStageGroup>();  // rows 0 .. W-1
 #pragma unroll
-        for (int m = 0; m < W - 1; ++m) widen8(xs[m * 32], ring[m]);
+        for (int m = 0; m < W - 1; ++m) ring[m] = xs[m * 32];
 #pragma unroll
         for (int u = 0; u < kVecRun; ++u) {
             if (u >= n) break;  // warp-uniform
@@ -313,24 +329,11 @@ __global__ void __launch_bounds__(kThreads, 4) paged_vec_kernel(const PagedArgs 
             const int64_t ins = shfl64(mine.ins, u);
             const uint4 xr = xs[(u + W - 1) * 32];
             if (active) *reinterpret_cast<uint4 *>(a.cache + ins + chan_off) = xr;
-            f32x2 xf[4];
-            widen8(xr, xf);
-            f32x2 acc[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                acc[q] = fma2(ring[0][q], wf[0][q], 0ull);
-#pragma unroll
-                for (int iw = 1; iw < W - 1; ++iw) acc[q] = fma2(ring[iw][q], wf[iw][q], acc[q]);
-                acc[q] = fma2(xf[q], wf[W - 1][q], acc[q]);
-            }
-            const uint4 o = finish8<SILU, RESID>(acc, xf);
+            const uint4 o = paged_row<W, SILU, RESID>(wpk, ring, xr);
             if (active) __stcs(reinterpret_cast<uint4 *>(a.out + (t0 + u) * a.os_t + c0), o);
 #pragma unroll
-            for (int m = 0; m < W - 2; ++m)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) ring[m][q] = ring[m + 1][q];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) ring[W - 2][q] = xf[q];
+            for (int m = 0; m < W - 2; ++m) ring[m] = ring[m + 1];
+            ring[W - 2] = xr;
         }
         return;
     }
@@ -338,14 +341,14 @@ __global__ void __launch_bounds__(kThreads, 4) paged_vec_kernel(const PagedArgs 
     // General path.  The cache taps of a group of tokens are loaded before
     // any of the group's stores, so their latencies overlap instead of
     // queueing behind the stores (which the compiler cannot prove disjoint).
-    constexpr int kGroup = W <= 4 ? 12 / (W - 1) : 2;  // 48 or 32 registers of taps
+    constexpr int kGroup = W <= 3 ? 4 : 2;  // at most 8 vectors of taps in flight
     cp_async_wait<0>();
 #pragma unroll 1
     for (int g = 0; g < n; g += kGroup) {
         uint4 cached[kGroup][W - 1];
 #pragma unroll
         for (int j = 0; j < kGroup; ++j) {
-            // g + j < 16 + 12 <= 32; lanes without a token carry an empty plan.
+            // g + j < 8 + 4 <= 32; lanes without a token carry an empty plan.
             const int kinds = __shfl_sync(kFullMask, mine.kinds, g + j);
 #pragma unroll
             for (int iw = 0; iw < W - 1; ++iw) {
@@ -364,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 4) paged_vec_kernel(const PagedArgs 
             const int64_t off_last = shfl64(mine.off[W - 1], u);
             const uint4 xr = xs[(u + W - 1) * 32];
             if (active && ins >= 0) *reinterpret_cast<uint4 *>(a.cache + ins + chan_off) = xr;
-            f32x2 acc[4] = {0ull, 0ull, 0ull, 0ull};
+            float acc[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
             for (int iw = 0; iw < W; ++iw) {
                 const int kind = (kinds >> (2 * iw)) & 3;
@@ -375,14 +378,11 @@ __global__ void __launch_bounds__(kThreads, 4) paged_vec_kernel(const PagedArgs 
                 // The token's own position comes from the cache only when its
                 // query start lies after it (inconsistent metadata).
                 else if (active) tap = *reinterpret_cast<const uint4 *>(a.cache + off_last + chan_off);
-                f32x2 tf[4];
-                widen8(tap, tf);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) acc[q] = fma2(tf[q], wf[iw][q], acc[q]);
+                for (int q = 0; q < 4; ++q)
+                    fma_bf16x2(acc[2 * q], acc[2 * q + 1], word_of(tap, q), word_of(wpk[iw], q));
             }
-            f32x2 xf[4];
-            widen8(xr, xf);
-            const uint4 o = finish8<SILU, RESID>(acc, xf);
+            const uint4 o = finish_row<SILU, RESID>(acc, xr);
             if (active) __stcs(reinterpret_cast<uint4 *>(a.out + (t0 + u) * a.os_t + c0), o);
         }
     }

@@ -3,7 +3,7 @@
 Outputs within 1e-2*|ref| + 2e-5, conv_state bit-exact, untouched regions
 (pad sequences, zero-length sequences, wider state columns, guard bands)
 bit-exact.  Sizes span several chunks and ragged tails of both kernels
-(channel-last chunks of 128 tokens; channel-first chunks of 2048 tokens for
+(channel-last chunks of 256 tokens; channel-first chunks of 8176 tokens for
 aligned rows and 256 for the strided fallback).
 """
 from __future__ import annotations
@@ -61,6 +61,34 @@ def test_config_large_prefill_full_size(layout):
 
 
 # ------------------------------------------------------------- edge cases ----
+
+def _bf16_sweep(lo: float, hi: float) -> torch.Tensor:
+    """Every finite bf16 value in [lo, hi], as a 1-D bf16 tensor."""
+    bits = torch.arange(0, 1 << 16, dtype=torch.int32).to(torch.int16)
+    vals = bits.view(torch.bfloat16)
+    f = vals.float()
+    return vals[torch.isfinite(f) & (f >= lo) & (f <= hi)]
+
+
+@pytest.mark.parametrize("layout", ["tokens_dim", "dim_tokens"])
+def test_silu_over_every_bf16_value(layout):
+    """A delta filter (last tap 1, no bias, zero prior) makes out = silu(x):
+    x runs through every finite bf16 value in [-30, 30], so the activation
+    is checked across its whole range, on both sides of every switch in its
+    evaluation."""
+    sweep = _bf16_sweep(-30.0, 30.0)
+    dim = 64
+    tokens = (sweep.numel() + dim - 1) // dim
+    case = wl.varlen_prefill(90, [tokens], dim, 4, num_cache_lines=1, layout=layout,
+                             has_init="none", use_bias=False, with_cache_indices=False,
+                             name=f"silu_sweep_{layout}")
+    flat = torch.zeros(dim * tokens, dtype=torch.bfloat16)
+    flat[: sweep.numel()] = sweep
+    case.x.copy_(flat.view(dim, tokens))
+    case.weight.zero_()
+    case.weight[:, -1] = 1.0
+    check(case)
+
 
 LENGTHS = [1, 2, 3, 4, 5, 127, 128, 129, 255, 0, 300, 31, 33]
 
