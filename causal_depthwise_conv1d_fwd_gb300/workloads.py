@@ -240,6 +240,89 @@ def config_decode(seed: int = 1002) -> DecodeCase:
     return decode(seed, 256, 8192, 4, num_lines=512, name="decode_256x8192")
 
 
+@dataclass
+class SpecDecodeCase:
+    """Speculative verify step: seqlen draft tokens per row, the state holding
+    history columns, and the page's optional spec-decoding buffers."""
+    name: str
+    x: torch.Tensor                          # (batch, dim, seqlen)
+    weight: torch.Tensor
+    bias: Optional[torch.Tensor]
+    conv_state: torch.Tensor                 # (num_lines, dim, state_len)
+    conv_state_indices: Optional[torch.Tensor]
+    num_accepted_tokens: Optional[torch.Tensor]      # int32 [batch], values >= 1
+    intermediate_conv_window: Optional[torch.Tensor]  # bf16 (batch, steps, dim, width-1)
+    output_state_indices: Optional[torch.Tensor]      # int32 (batch, steps)
+    activation: Optional[str]
+    pad_slot_id: int = PAD_SLOT_ID
+
+    def kwargs(self) -> Dict:
+        return dict(x=self.x, conv_state=self.conv_state, weight=self.weight,
+                    bias=self.bias, activation=self.activation,
+                    conv_state_indices=self.conv_state_indices,
+                    num_accepted_tokens=self.num_accepted_tokens,
+                    intermediate_conv_window=self.intermediate_conv_window,
+                    output_state_indices=self.output_state_indices,
+                    pad_slot_id=self.pad_slot_id)
+
+
+def spec_decode(seed: int, batch: int, dim: int, width: int = 4, seqlen: int = 4, *,
+                num_lines: Optional[int] = None, history: int = 4,
+                with_accepted: bool = True, with_intermediate: bool = False,
+                with_output_indices: bool = False, steps: Optional[int] = None,
+                skip_frac: float = 0.25, pad_positions=(), use_bias: bool = True,
+                activation: Optional[str] = "silu", std: float = STD,
+                name: str = "spec_decode") -> SpecDecodeCase:
+    """Random verify step.  The state keeps width-1+history columns, so up to
+    history+1 accepted tokens can be addressed; without intermediate or
+    output buffers it is widened to the width-2+seqlen columns the in-place
+    shift writes.  Input lines are a random subset of the pool; output lines
+    (when asked for) are drawn from the rest, about skip_frac of them -1.
+    The intermediate buffer starts as random values, so untouched entries are
+    recognisable."""
+    g = _gen(seed)
+    num_lines = 3 * batch * max(1, seqlen) if num_lines is None else num_lines
+    state_len = width - 1 + history
+    if not (with_intermediate or with_output_indices):
+        state_len = max(state_len, width - 2 + seqlen)
+    steps = seqlen if steps is None else steps
+    x = randn_bf16((batch, dim, seqlen), g, std)
+    weight = randn_bf16((dim, width), g, std)
+    bias = randn_bf16((dim,), g, std) if use_bias else None
+    conv_state = make_states(num_lines, dim, state_len, "dim_contiguous", g, std)
+    perm = torch.randperm(num_lines, generator=g).to(torch.int32)
+    idx = perm[:batch].clone()
+    for p in pad_positions:
+        idx[p] = PAD_SLOT_ID
+    nacc = None
+    if with_accepted:
+        nacc = torch.randint(1, history + 2, (batch,), generator=g, dtype=torch.int32)
+    inter = None
+    if with_intermediate:
+        inter = randn_bf16((batch, width - 1, steps, dim), g, std).permute(0, 2, 3, 1)
+    oidx = None
+    if with_output_indices:
+        pool = perm[batch:]
+        if pool.numel() < batch * steps:
+            raise ValueError("num_lines too small for distinct output lines")
+        oidx = pool[: batch * steps].reshape(batch, steps).clone()
+        drop = torch.rand((batch, steps), generator=g) < skip_frac
+        oidx[drop] = -1
+    return SpecDecodeCase(name=name, x=x, weight=weight, bias=bias, conv_state=conv_state,
+                          conv_state_indices=idx, num_accepted_tokens=nacc,
+                          intermediate_conv_window=inter, output_state_indices=oidx,
+                          activation=activation)
+
+
+def config_spec_decode(seed: int = 1005) -> SpecDecodeCase:
+    """Speculative verify: 64 rows x 4 draft tokens, dim 8192, W 4, history of
+    4 columns, num_accepted_tokens in [1, 5], per-step windows written to an
+    intermediate buffer and scattered to output state lines."""
+    return spec_decode(seed, 64, 8192, 4, 4, history=4, with_accepted=True,
+                       with_intermediate=True, with_output_indices=True,
+                       name="spec_verify_64x4_dim8192")
+
+
 # ----------------------------------------------------------------- paged ----
 
 @dataclass

@@ -46,6 +46,11 @@ def _lib():
             _P, _I64, _I64, _I64, _P, _I64, _I64, _I64, _P, _I64, _I64, _P,
             _P, _I64, _I64, _I64, _I32, _P, _I32, _I32, _I32,
             _I32, _I32, _I32, _P]
+        lib.oracle_ccv_update_spec.argtypes = [
+            _P, _I64, _I64, _I64, _P, _I64, _I64, _I64, _P, _I64, _I64, _P,
+            _P, _I64, _I64, _I64, _I32, _I32, _P, _P,
+            _P, _I64, _I64, _I64, _I64, _P, _I64, _I64,
+            _I32, _I32, _I32, _I32, _I32, _I32, _P]
         lib.oracle_paged_sconv_seq_metadata.argtypes = [_P, _I32, _I32, _I32, _P, _P]
         lib.oracle_paged_sconv_fwd.argtypes = [
             _P, _I64, _P, _I64, _I64, _I64, _I32, _I32, _I32, _I32,
@@ -53,7 +58,7 @@ def _lib():
             _P, _I32, _I32, _I32, _I32, _I32, _I32, _P]
         lib.oracle_f32_to_bf16.argtypes = [_P, _P, _I64]
         lib.oracle_silu_f32.argtypes = [_P, _P, _I64]
-        for name in ("oracle_ccv_fwd", "oracle_ccv_update",
+        for name in ("oracle_ccv_fwd", "oracle_ccv_update", "oracle_ccv_update_spec",
                      "oracle_paged_sconv_seq_metadata", "oracle_paged_sconv_fwd"):
             getattr(lib, name).restype = ctypes.c_int
         _LIB = lib
@@ -152,6 +157,48 @@ def ccv_update(x, conv_state, weight, bias=None, activation=None,
         _ptr(weight), weight.stride(0), weight.stride(1), _ptr(bias),
         _ptr(conv_state), ss[0], ss[1], ss[2], conv_state.shape[0],
         _ptr(idx), batch, dim, seqlen, width, pad_slot_id, silu, ctypes.byref(err))
+    res = out3.squeeze(-1) if squeeze else out3
+    return res, err.value
+
+
+def ccv_update_spec(x, conv_state, weight, bias=None, activation=None,
+                    conv_state_indices=None, num_accepted_tokens=None,
+                    intermediate_conv_window=None, output_state_indices=None,
+                    pad_slot_id=-1, out=None):
+    """Decode / speculative-verify update with the page's spec-decoding extras.
+
+    x is (batch, dim, seqlen) (or (batch, dim)); out defaults to x.
+    num_accepted_tokens: int32 [batch] or None; intermediate_conv_window:
+    bf16 (batch, >= seqlen, dim, width-1) or None, written; output_state_indices:
+    int32 (batch, >= seqlen) or None.  Returns (out, err_count).
+    """
+    _check(x, torch.bfloat16, "x")
+    squeeze = x.dim() == 2
+    x3 = x.unsqueeze(-1) if squeeze else x
+    if out is None:
+        out3 = x3
+    else:
+        out3 = out.unsqueeze(-1) if out.dim() == 2 else out
+    batch, dim, seqlen = x3.shape
+    width = weight.shape[1]
+    silu = _silu_flag(activation)
+    # keep converted index tensors alive until the call returns
+    idx = None if conv_state_indices is None else conv_state_indices.to(torch.int32).contiguous()
+    nacc = None if num_accepted_tokens is None else num_accepted_tokens.to(torch.int32).contiguous()
+    oidx = None if output_state_indices is None else output_state_indices.to(torch.int32)
+    inter = intermediate_conv_window
+    if inter is not None:
+        _check(inter, torch.bfloat16, "intermediate_conv_window")
+    ist = inter.stride() if inter is not None else (0, 0, 0, 0)
+    ost = oidx.stride() if oidx is not None else (0, 0)
+    ss = conv_state.stride()
+    err = ctypes.c_int(0)
+    _lib().oracle_ccv_update_spec(
+        _ptr(x3), *x3.stride(), _ptr(out3), *out3.stride(),
+        _ptr(weight), weight.stride(0), weight.stride(1), _ptr(bias),
+        _ptr(conv_state), ss[0], ss[1], ss[2], conv_state.shape[0], conv_state.shape[2],
+        _ptr(idx), _ptr(nacc), _ptr(inter), *ist, _ptr(oidx), *ost,
+        batch, dim, seqlen, width, pad_slot_id, silu, ctypes.byref(err))
     res = out3.squeeze(-1) if squeeze else out3
     return res, err.value
 

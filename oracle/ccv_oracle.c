@@ -217,6 +217,90 @@ int oracle_ccv_update(const uint16_t *x, int64_t xs_b, int64_t xs_d, int64_t xs_
     return 0;
 }
 
+/*
+ * oracle_ccv_update_spec -- [P1] `causal_conv1d_update` with its
+ * speculative-decoding extras (`num_accepted_tokens`,
+ * `intermediate_conv_window`, `output_state_indices`).
+ *
+ * Row b reads its window from state columns off .. off+W-2 of its line, where
+ * off = num_accepted_tokens[b] - 1 (0 without it): [P1] rolls the state as
+ * [history.., draft1..draftN] and a verify step that accepted k drafts starts
+ * k-1 columns in.  With u = those W-1 columns ++ x[b, c, 0..seqlen-1]:
+ *   out[b, c, t] = act(bias[c] + sum_k w[c,k] * u[t+k])
+ * and the window after token t is u[t+1 .. t+W-1].  For each t that window
+ * is written to intermediate_conv_window[b, t, c, 0..W-2] (indexed by the
+ * batch position, not the state line) and, when output_state_indices[b, t]
+ * >= 0, to columns 0..W-2 of that state line.  When neither buffer is given
+ * the state is shifted in place instead, as in the plain update:
+ *   conv_state[line, c, j] = u[1 + j],  j = 0 .. W-3+seqlen.
+ * A row whose offset leaves no room for W-1 columns (off < 0 or off+W-1 >
+ * state_len), or an output line outside the pool, is counted in err_count
+ * and skipped (the row, or that one window write).  Output lines must not be
+ * lines that other rows of the same call read.
+ */
+int oracle_ccv_update_spec(const uint16_t *x, int64_t xs_b, int64_t xs_d, int64_t xs_t,
+                           uint16_t *out, int64_t os_b, int64_t os_d, int64_t os_t,
+                           const uint16_t *weight, int64_t ws_dim, int64_t ws_w,
+                           const uint16_t *bias,
+                           uint16_t *conv_state, int64_t ss_line, int64_t ss_dim, int64_t ss_tok,
+                           int num_cache_lines, int state_len,
+                           const int32_t *conv_state_indices, const int32_t *num_accepted_tokens,
+                           uint16_t *inter, int64_t is_b, int64_t is_t, int64_t is_d, int64_t is_w,
+                           const int32_t *out_state_idx, int64_t ois_b, int64_t ois_t,
+                           int batch, int dim, int seqlen,
+                           int width, int pad_slot_id, int silu, int *err_count) {
+    const int W = width;
+    const int shift = inter == NULL && out_state_idx == NULL;
+    uint16_t *u_bits = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)(W - 1 + seqlen));
+    for (int b = 0; b < batch; b++) {
+        int line = conv_state_indices ? conv_state_indices[b] : b;
+        if (line == pad_slot_id) continue;
+        if (line < 0 || line >= num_cache_lines) {
+            count_error(err_count);
+            continue;
+        }
+        int off = num_accepted_tokens ? num_accepted_tokens[b] - 1 : 0;
+        if (off < 0 || off + W - 1 > state_len) {
+            count_error(err_count);
+            continue;
+        }
+        for (int t = 0; t < seqlen && out_state_idx; t++) {
+            int o = out_state_idx[b * ois_b + t * ois_t];
+            if (o >= num_cache_lines) count_error(err_count);
+        }
+        for (int c = 0; c < dim; c++) {
+            for (int j = 0; j < W - 1; j++)
+                u_bits[j] = conv_state[line * ss_line + c * ss_dim + (off + j) * ss_tok];
+            for (int t = 0; t < seqlen; t++)
+                u_bits[W - 1 + t] = x[b * xs_b + c * xs_d + t * xs_t];
+
+            float bc = bias ? bf16_to_f32(bias[c]) : 0.0f;
+            for (int t = 0; t < seqlen; t++) {
+                float acc = bc;
+                for (int k = 0; k < W; k++)
+                    acc = acc + bf16_to_f32(weight[c * ws_dim + k * ws_w]) *
+                                    bf16_to_f32(u_bits[t + k]);
+                if (silu) acc = silu_f32(acc);
+                out[b * os_b + c * os_d + t * os_t] = f32_to_bf16(acc);
+                for (int j = 0; j < W - 1; j++) {
+                    uint16_t v = u_bits[t + 1 + j];
+                    if (inter) inter[b * is_b + t * is_t + c * is_d + j * is_w] = v;
+                    if (out_state_idx) {
+                        int o = out_state_idx[b * ois_b + t * ois_t];
+                        if (o >= 0 && o < num_cache_lines)
+                            conv_state[o * ss_line + c * ss_dim + j * ss_tok] = v;
+                    }
+                }
+            }
+            if (shift)
+                for (int j = 0; j < W - 2 + seqlen; j++)
+                    conv_state[line * ss_line + c * ss_dim + j * ss_tok] = u_bits[1 + j];
+        }
+    }
+    free(u_bits);
+    return 0;
+}
+
 /* ------------------------------------------------------ paged metadata ---- */
 
 /*

@@ -432,6 +432,130 @@ def test_decode_matches_reference_formulation():
         assert_bf16_close(out[b][:, None], ref)
 
 
+# -------------------------------------------------------- spec decoding ----
+
+def _spec_prior(case, b):
+    """(dim, W-1) window row b starts from: state columns off .. off+W-2."""
+    W = case.weight.shape[1]
+    line = int(case.conv_state_indices[b])
+    off = int(case.num_accepted_tokens[b]) - 1 if case.num_accepted_tokens is not None else 0
+    return case.conv_state[line, :, off:off + W - 1].clone()
+
+
+def _run_spec(case):
+    pool = case.conv_state.clone()
+    inter = None if case.intermediate_conv_window is None else case.intermediate_conv_window.clone()
+    x = case.x.clone()
+    out, err = oracle.ccv_update_spec(x, pool, case.weight, case.bias, case.activation,
+                                      case.conv_state_indices, case.num_accepted_tokens,
+                                      inter, case.output_state_indices, case.pad_slot_id)
+    return out, pool, inter, err
+
+
+@pytest.mark.parametrize("width", [2, 3, 4, 5])
+def test_spec_without_extras_equals_plain_update(width):
+    """No accepted-token offset and no buffers: the plain multi-token update."""
+    case = wl.spec_decode(400 + width, 5, 24, width, 3, with_accepted=False, history=1,
+                          pad_positions=(2,))
+    out_s, pool_s, _, err_s = _run_spec(case)
+    pool_p = case.conv_state.clone()
+    out_p, err_p = oracle.ccv_update(case.x.clone(), pool_p, case.weight, case.bias,
+                                     case.activation, case.conv_state_indices, -1)
+    assert err_s == err_p == 0
+    assert torch.equal(out_s.view(torch.int16), out_p.view(torch.int16))
+    assert torch.equal(pool_s.view(torch.int16), pool_p.view(torch.int16))
+
+
+@pytest.mark.parametrize("width", [2, 3, 4, 5])
+def test_spec_outputs_match_reference_formulation(width):
+    """Outputs against F.conv1d on the window at the accepted-token offset."""
+    case = wl.spec_decode(410 + width, 6, 32, width, 4, history=3, with_intermediate=True,
+                          with_output_indices=True)
+    out, _, _, err = _run_spec(case)
+    assert err == 0
+    for b in range(6):
+        ref = r1_reference(case.x[b], case.weight, case.bias, _spec_prior(case, b), True)
+        assert_bf16_close(out[b], ref)
+
+
+@pytest.mark.parametrize("width", [2, 3, 4, 5])
+def test_spec_windows_and_output_lines_are_last_inputs(width):
+    """After token t the window is the last W-1 inputs of prior ++ x[:t+1]:
+    it lands in the intermediate buffer at (b, t) and in output line
+    output_state_indices[b, t] (columns 0..W-2); nothing else changes."""
+    seqlen, steps = 3, 5
+    case = wl.spec_decode(420 + width, 4, 16, width, seqlen, history=2, steps=steps,
+                          with_intermediate=True, with_output_indices=True, skip_frac=0.3)
+    _, pool, inter, err = _run_spec(case)
+    assert err == 0
+    exp_pool = case.conv_state.clone()
+    exp_inter = case.intermediate_conv_window.clone()
+    for b in range(4):
+        u = torch.cat([_spec_prior(case, b), case.x[b]], dim=1)
+        for t in range(seqlen):
+            win = u[:, t + 1:t + width]
+            exp_inter[b, t] = win
+            o = int(case.output_state_indices[b, t])
+            if o >= 0:
+                exp_pool[o, :, :width - 1] = win
+    assert torch.equal(inter.view(torch.int16), exp_inter.view(torch.int16))
+    assert torch.equal(pool.view(torch.int16), exp_pool.view(torch.int16))
+
+
+@pytest.mark.parametrize("width", [2, 3, 4, 5])
+def test_spec_verify_equals_successive_single_token_updates(width):
+    """A verify step over N drafts gives the outputs and per-step windows of N
+    single-token decode updates started from the offset window."""
+    seqlen = 4
+    case = wl.spec_decode(430 + width, 3, 16, width, seqlen, history=3,
+                          with_intermediate=True)
+    out, _, inter, err = _run_spec(case)
+    assert err == 0
+    for b in range(3):
+        pool = _spec_prior(case, b).unsqueeze(0).contiguous()
+        for t in range(seqlen):
+            xt = case.x[b:b + 1, :, t].clone()
+            o1, e1 = oracle.ccv_update(xt, pool, case.weight, case.bias, case.activation,
+                                       None, -1)
+            assert e1 == 0
+            assert torch.equal(out[b, :, t].view(torch.int16), o1[0].view(torch.int16))
+            assert torch.equal(inter[b, t].view(torch.int16), pool[0].view(torch.int16))
+
+
+@pytest.mark.parametrize("width", [2, 4, 5])
+def test_spec_shift_with_offset_is_closed_form(width):
+    """Offset but no buffers: columns [0, W-2+seqlen) of the line become
+    (window ++ x)[1:]; the other columns and lines stay."""
+    seqlen = 3
+    case = wl.spec_decode(440 + width, 4, 16, width, seqlen, history=3)
+    _, pool, _, err = _run_spec(case)
+    assert err == 0
+    exp = case.conv_state.clone()
+    for b in range(4):
+        line = int(case.conv_state_indices[b])
+        u = torch.cat([_spec_prior(case, b), case.x[b]], dim=1)
+        exp[line, :, :width - 2 + seqlen] = u[:, 1:]
+    assert torch.equal(pool.view(torch.int16), exp.view(torch.int16))
+
+
+def test_spec_invalid_offsets_and_output_lines_are_counted():
+    case = wl.spec_decode(450, 4, 16, 4, 2, history=1, with_output_indices=True,
+                          skip_frac=0.0)
+    case.num_accepted_tokens[1] = 0                   # offset -1
+    case.num_accepted_tokens[2] = 3                   # offset 2: needs 5 columns, has 4
+    case.output_state_indices[3, 1] = case.conv_state.shape[0]   # outside the pool
+    out, pool, _, err = _run_spec(case)
+    assert err > 0
+    for b in (1, 2):                                  # skipped rows: out is still x
+        assert torch.equal(out[b].view(torch.int16), case.x[b].view(torch.int16))
+        for t in range(2):
+            o = int(case.output_state_indices[b, t])
+            assert torch.equal(pool[o].view(torch.int16), case.conv_state[o].view(torch.int16))
+    o = int(case.output_state_indices[3, 0])          # the valid write of row 3 happened
+    u = torch.cat([_spec_prior(case, 3), case.x[3]], dim=1)
+    assert torch.equal(pool[o, :, :3].view(torch.int16), u[:, 1:4].view(torch.int16))
+
+
 # ----------------------------------------------------------------- paged ----
 
 def _small_paged(seed, lengths, starts, **kw):

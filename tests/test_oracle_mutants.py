@@ -47,6 +47,12 @@ MUTANTS = [
     ("paged_pad_not_masked", "int real = slot_mapping[t] >= 0;", "int real = 1;"),
     ("metadata_strict", "if (query_start_loc[j] <= t) owner = j;",
      "if (query_start_loc[j] < t) owner = j;"),
+    ("spec_offset_is_count", "num_accepted_tokens[b] - 1 : 0", "num_accepted_tokens[b] : 0"),
+    ("spec_window_lags", "uint16_t v = u_bits[t + 1 + j];", "uint16_t v = u_bits[t + j];"),
+    ("spec_never_shifts", "const int shift = inter == NULL && out_state_idx == NULL;",
+     "const int shift = 0;"),
+    ("spec_output_column_shifted", "conv_state[o * ss_line + c * ss_dim + j * ss_tok] = v;",
+     "conv_state[o * ss_line + c * ss_dim + (j + 1) * ss_tok] = v;"),
 ]
 
 
