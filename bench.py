@@ -79,6 +79,28 @@ def decode_bytes(case) -> int:
     return rows * per_row + dim * W * 2 + dim * 2 + 4 * B
 
 
+def spec_bytes(case) -> int:
+    """Speculative verify: per non-pad row x read + out write + the window
+    read + the intermediate windows + the output-line windows (+ the shifted
+    columns when no buffer is given), plus weights, bias and indices."""
+    B, dim, S = case.x.shape
+    W = case.weight.shape[1]
+    rows = [b for b in range(B) if int(case.conv_state_indices[b]) != case.pad_slot_id]
+    per_row = dim * 2 * (2 * S + (W - 1))
+    total = 0
+    for b in rows:
+        total += per_row
+        if case.intermediate_conv_window is not None:
+            total += S * dim * (W - 1) * 2
+        if case.output_state_indices is not None:
+            total += int((case.output_state_indices[b, :S] >= 0).sum()) * dim * (W - 1) * 2
+        if case.intermediate_conv_window is None and case.output_state_indices is None:
+            total += dim * (W - 2 + S) * 2
+    idx_bytes = 4 * B * (1 + (case.num_accepted_tokens is not None)
+                         + (S if case.output_state_indices is not None else 0))
+    return total + dim * W * 2 + dim * 2 + idx_bytes
+
+
 _PAGED_BYTES = {}
 
 
@@ -462,6 +484,55 @@ def decode_graph_us(dev_args, replays=200):
     return a.elapsed_time(b) * 1e3 / replays
 
 
+def spec_verify_timing(dev, rank, calls=50):
+    """The speculative-verify update (not part of the step): us per call
+    L2-cold (a write larger than L2 between calls, outside the timed
+    window) and as warm CUDA-graph replay."""
+    import causal_depthwise_conv1d_fwd_gb300 as ccv
+    from causal_depthwise_conv1d_fwd_gb300 import workloads as wl
+
+    c = wl.config_spec_decode(1005 + 100 * rank)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in c.kwargs().items()}
+    src = c.intermediate_conv_window
+    inter = torch.empty_strided(src.shape, src.stride(), dtype=src.dtype, device=dev)
+    inter.copy_(src)
+    d["intermediate_conv_window"] = inter
+    launch = ccv.prepare_ccv_update_spec(**d)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        launch(stream.cuda_stream)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(calls)]
+    for a, b in evs:
+        flush.zero_()
+        a.record()
+        launch(stream.cuda_stream)
+        b.record()
+    torch.cuda.synchronize()
+    cold = sorted(a.elapsed_time(b) * 1e3 for a, b in evs)[calls // 2]
+    s = torch.cuda.Stream()
+    s.wait_stream(stream)
+    with torch.cuda.stream(s):
+        launch(s.cuda_stream)
+    stream.wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        launch(torch.cuda.current_stream().cuda_stream)
+    for _ in range(10):
+        g.replay()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(200):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    nbytes = spec_bytes(c)
+    return {"workload": c.name, "kernel": "update_kernel", "bytes": nbytes,
+            "us_l2_cold": round(cold, 2), "gbs_l2_cold": round(nbytes / (cold * 1e-6) / 1e9, 1),
+            "us_graph_warm": round(a.elapsed_time(b) * 1e3 / 200, 2)}
+
+
 def run_ours(args):
     import causal_depthwise_conv1d_fwd_gb300 as ccv  # noqa: F401
     from causal_depthwise_conv1d_fwd_gb300 import _lib
@@ -528,6 +599,7 @@ def run_ours(args):
     e2e_s = max_over_ranks(e2e_s, dev)
     e2e_value = whole_job_rate(step_bytes, e2e_steps, world, e2e_s) / 1e9
     graph_us = decode_graph_us(dev_args)
+    spec = spec_verify_timing(dev, rank)
 
     if rank != 0:
         return
@@ -566,6 +638,7 @@ def run_ours(args):
         "mtok_per_s_prefill": round(mtok, 1),
         "decode_us_per_call": parts_out["decode"]["us_per_call_l2_cold"],
         "decode_us_per_call_graph_warm": round(graph_us, 2),
+        "spec_verify": spec,
         "parts": parts_out,
         "roofline": {"bound": "hbm", "kernel": dominant.kernel, "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",

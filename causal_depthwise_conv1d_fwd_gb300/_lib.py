@@ -26,6 +26,10 @@ SIGNATURES = {
     "ccv_update": ([P, I64, I64, I64, P, I64, I64, I64, P, I64, I64, P,
                     P, I64, I64, I64, I32, I32, P, I32, I32, I32,
                     I32, I32, I32, P, P], I32),
+    "ccv_update_spec": ([P, I64, I64, I64, P, I64, I64, I64, P, I64, I64, P,
+                         P, I64, I64, I64, I32, I32, P, P,
+                         P, I64, I64, I64, I64, I32, P, I64, I64, I32,
+                         I32, I32, I32, I32, I32, I32, P, P], I32),
     "paged_sconv_seq_metadata": ([P, I32, I32, I32, P, P, I32, P], I32),
     "paged_sconv_fwd": ([P, I64, P, I64, I64, I64, I32, I32, I32, I32,
                          P, I64, I64, P, I64, P, P, P, P, I64, I32, I32,

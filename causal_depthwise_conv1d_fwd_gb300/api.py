@@ -189,6 +189,78 @@ def prepare_ccv_update(x, conv_state, weight, bias=None, activation=None,
                   (x3, out3, weight, bias, conv_state, idx, err_count))
 
 
+def ccv_update_spec(x: torch.Tensor, conv_state: torch.Tensor, weight: torch.Tensor,
+                    bias: Optional[torch.Tensor] = None, activation=None,
+                    conv_state_indices: Optional[torch.Tensor] = None,
+                    num_accepted_tokens: Optional[torch.Tensor] = None,
+                    intermediate_conv_window: Optional[torch.Tensor] = None,
+                    output_state_indices: Optional[torch.Tensor] = None,
+                    pad_slot_id: int = PAD_SLOT_ID, out: Optional[torch.Tensor] = None,
+                    err_count: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Decode / speculative-verify step with the spec-decoding extras.
+
+    num_accepted_tokens: int32 [batch] (window read at column value-1);
+    intermediate_conv_window: bf16 (batch, steps >= seqlen, dim, width-1),
+    receives the window after every token; output_state_indices: int32
+    (batch, steps >= seqlen), the state line each step's window is written
+    to (-1: none).  With either buffer the state is not shifted in place.
+    """
+    return prepare_ccv_update_spec(x, conv_state, weight, bias, activation, conv_state_indices,
+                                   num_accepted_tokens, intermediate_conv_window,
+                                   output_state_indices, pad_slot_id, out, err_count)(stream)
+
+
+def prepare_ccv_update_spec(x, conv_state, weight, bias=None, activation=None,
+                            conv_state_indices=None, num_accepted_tokens=None,
+                            intermediate_conv_window=None, output_state_indices=None,
+                            pad_slot_id=PAD_SLOT_ID, out=None, err_count=None) -> Launch:
+    """Validate and marshal a ccv_update_spec call once; returns a reusable Launch."""
+    _need_cuda(x, "x", torch.bfloat16)
+    _need_cuda(conv_state, "conv_state", torch.bfloat16)
+    _need_cuda(weight, "weight", torch.bfloat16)
+    _need_cuda(bias, "bias", torch.bfloat16)
+    squeeze = x.dim() == 2
+    x3 = x.unsqueeze(-1) if squeeze else x
+    if x3.dim() != 3:
+        raise ValueError("x must be (batch, dim) or (batch, dim, seqlen)")
+    batch, dim, seqlen = x3.shape
+    width = weight.shape[1]
+    if weight.shape[0] != dim or conv_state.dim() != 3 or conv_state.shape[1] != dim:
+        raise ValueError("weight / conv_state do not match dim")
+    if out is None:
+        out3 = x3
+    else:
+        _need_cuda(out, "out", torch.bfloat16)
+        out3 = out.unsqueeze(-1) if out.dim() == 2 else out
+        if out3.shape != x3.shape:
+            raise ValueError("out must have x's shape")
+    idx = _index_vector(conv_state_indices, "conv_state_indices", torch.int32, batch)
+    nacc = _index_vector(num_accepted_tokens, "num_accepted_tokens", torch.int32, batch)
+    inter = intermediate_conv_window
+    _need_cuda(inter, "intermediate_conv_window", torch.bfloat16)
+    if inter is not None and (inter.dim() != 4 or inter.shape[0] != batch or
+                              inter.shape[2] != dim or inter.shape[3] != width - 1):
+        raise ValueError("intermediate_conv_window must be (batch, steps, dim, width-1)")
+    oidx = output_state_indices
+    _need_cuda(oidx, "output_state_indices", torch.int32)
+    if oidx is not None and (oidx.dim() != 2 or oidx.shape[0] != batch):
+        raise ValueError("output_state_indices must be (batch, steps)")
+    _need_cuda(err_count, "err_count", torch.int32)
+    ss = conv_state.stride()
+    ist = inter.stride() if inter is not None else (0, 0, 0, 0)
+    ost = oidx.stride() if oidx is not None else (0, 0)
+    args = (_ptr(x3), *x3.stride(), _ptr(out3), *out3.stride(),
+            _ptr(weight), weight.stride(0), weight.stride(1), _ptr(bias),
+            _ptr(conv_state), ss[0], ss[1], ss[2], conv_state.shape[0], conv_state.shape[2],
+            _ptr(idx), _ptr(nacc),
+            _ptr(inter), *ist, inter.shape[1] if inter is not None else 0,
+            _ptr(oidx), *ost, oidx.shape[1] if oidx is not None else 0,
+            batch, dim, seqlen, width, pad_slot_id, _silu_flag(activation), _ptr(err_count))
+    result = out3.squeeze(-1) if squeeze else out3
+    return Launch("ccv_update_spec", args, result,
+                  (x3, out3, weight, bias, conv_state, idx, nacc, inter, oidx, err_count))
+
+
 def paged_sconv_seq_metadata(query_start_loc: torch.Tensor, num_reqs: int,
                              num_actual_tokens: int, seq_idx_out: torch.Tensor,
                              query_start_out: torch.Tensor,

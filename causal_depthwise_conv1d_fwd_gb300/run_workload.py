@@ -5,7 +5,8 @@ Used to give a profiler a small, self-contained program:
     python -m causal_depthwise_conv1d_fwd_gb300.run_workload --part prefill_tokens_dim --reps 3
 
 Parts: prefill_tokens_dim, prefill_dim_tokens (4 x 4096 tokens, dim 8192),
-decode (256 x 8192), paged (H16 x ws128, 32 requests; metadata + conv).
+decode (256 x 8192), paged (H16 x ws128, 32 requests; metadata + conv),
+spec (speculative verify, 64 rows x 4 drafts, dim 8192).
 The process exits 0 after a device synchronize; it times nothing.
 """
 from __future__ import annotations
@@ -17,7 +18,7 @@ import torch
 from . import api
 from . import workloads as wl
 
-PARTS = ("prefill_tokens_dim", "prefill_dim_tokens", "decode", "paged")
+PARTS = ("prefill_tokens_dim", "prefill_dim_tokens", "decode", "paged", "spec")
 
 
 def _dev(kwargs, dev):
@@ -50,6 +51,15 @@ def make_launch(part: str, dev):
             meta()
             conv()
         return run
+    if part == "spec":
+        c = wl.config_spec_decode()
+        d = _dev(c.kwargs(), dev)
+        src = c.intermediate_conv_window
+        inter = torch.empty_strided(src.shape, src.stride(), dtype=src.dtype, device=dev)
+        inter.copy_(src)
+        d["intermediate_conv_window"] = inter
+        launch = api.prepare_ccv_update_spec(**d)
+        return lambda: launch()
     raise ValueError(f"unknown part {part!r}; choose from {PARTS}")
 
 

@@ -286,7 +286,9 @@ def spec_decode(seed: int, batch: int, dim: int, width: int = 4, seqlen: int = 4
     if not (with_intermediate or with_output_indices):
         state_len = max(state_len, width - 2 + seqlen)
     steps = seqlen if steps is None else steps
-    x = randn_bf16((batch, dim, seqlen), g, std)
+    # channels contiguous (x.stride(1) == 1), the layout the page's update
+    # wrapper asserts
+    x = randn_bf16((batch, seqlen, dim), g, std).transpose(1, 2)
     weight = randn_bf16((dim, width), g, std)
     bias = randn_bf16((dim,), g, std) if use_bias else None
     conv_state = make_states(num_lines, dim, state_len, "dim_contiguous", g, std)

@@ -105,7 +105,8 @@ int ccv_fwd(const void *x, int64_t x_stride_dim, int64_t x_stride_tok,
  * ccv_update -- decode step: causal conv over `seqlen` new tokens per row
  * with the row's conv_state as the window prefix, state shifted in place.
  * tokenspeed causal_conv1d.py, `causal_conv1d_update` and
- * `_causal_conv1d_update_kernel` (non-speculative path).
+ * `_causal_conv1d_update_kernel` (non-speculative path; ccv_update_spec
+ * below adds the speculative-decoding extras).
  *
  * x, out        (batch, dim, seqlen) with strides (b, d, t); out may be
  *               exactly x (same pointer and strides: in-place, as the page's
@@ -127,6 +128,49 @@ int ccv_update(const void *x, int64_t x_stride_b, int64_t x_stride_dim, int64_t 
                const int32_t *conv_state_indices, int batch, int dim, int seqlen,
                int width, int pad_slot_id, int silu, int *err_count,
                ccv_stream_t stream);
+
+/*
+ * ccv_update_spec -- ccv_update with the speculative-decoding extras of
+ * tokenspeed causal_conv1d.py, `causal_conv1d_update` (num_accepted_tokens,
+ * intermediate_conv_window, output_state_indices).  Every argument shared
+ * with ccv_update means the same.
+ *
+ * num_accepted_tokens  int32 [batch] or NULL.  Row b reads its window from
+ *               state columns off .. off+width-2, off = num_accepted_tokens[b]
+ *               - 1 (0 when NULL): after a verify step that kept k drafts the
+ *               state holds [history.., drafts..] and the window starts k-1
+ *               columns in.  A row with off < 0 or off+width-1 > state_len is
+ *               skipped and counted in err_count.
+ * intermediate_conv_window  bf16 or NULL, element (b, step, c, j) at
+ *               b*i_stride_b + step*i_stride_step + c*i_stride_dim +
+ *               j*i_stride_win, inter_steps >= seqlen steps: after token t
+ *               it receives the window u[t+1 .. t+width-1] (the last width-1
+ *               inputs), indexed by batch position, not by state line.  Must
+ *               not overlap x, out or conv_state.
+ * output_state_indices  int32 or NULL, element (b, step) at b*oi_stride_b +
+ *               step*oi_stride_step, oidx_steps >= seqlen: when the entry for
+ *               (b, t) is >= 0 the same window is written to columns
+ *               0..width-2 of that state line (a line outside the pool is
+ *               counted and skipped).  Output lines must not be lines that
+ *               other rows of the same call read (they would race).
+ * When either buffer is given the state line is NOT shifted in place and
+ * state_len >= width-1 suffices; otherwise the line is shifted exactly as
+ * in ccv_update (state_len >= width-2+seqlen).  inter_steps or oidx_steps
+ * below seqlen gives CCV_ERR_CAPACITY.
+ */
+int ccv_update_spec(const void *x, int64_t x_stride_b, int64_t x_stride_dim, int64_t x_stride_tok,
+                    void *out, int64_t out_stride_b, int64_t out_stride_dim,
+                    int64_t out_stride_tok, const void *weight, int64_t w_stride_dim,
+                    int64_t w_stride_w, const void *bias,
+                    void *conv_state, int64_t s_stride_line, int64_t s_stride_dim,
+                    int64_t s_stride_tok, int num_cache_lines, int state_len,
+                    const int32_t *conv_state_indices, const int32_t *num_accepted_tokens,
+                    void *intermediate_conv_window, int64_t i_stride_b, int64_t i_stride_step,
+                    int64_t i_stride_dim, int64_t i_stride_win, int inter_steps,
+                    const int32_t *output_state_indices, int64_t oi_stride_b,
+                    int64_t oi_stride_step, int oidx_steps,
+                    int batch, int dim, int seqlen, int width, int pad_slot_id, int silu,
+                    int *err_count, ccv_stream_t stream);
 
 /*
  * paged_sconv_seq_metadata -- per-token request id and first x-row.

@@ -17,6 +17,7 @@ from causal_depthwise_conv1d_fwd_gb300 import _lib, build
 
 OK, NULLP, WIDTH, SIZE, STATE, ALIAS, STRIDE, RANGE, CAP, ARG = 0, -1, -2, -3, -4, -5, -6, -7, -8, -9
 A, B, C = 0x10000, 0x2000000, 0x8000000  # fake 16-byte-aligned device addresses, far apart
+D, E = 0x20000000, 0x40000000
 
 
 @pytest.fixture(scope="module")
@@ -28,7 +29,7 @@ def lib():
 def test_every_declared_function_is_exported(lib):
     names = _lib.declared_functions()
     assert set(names) == {"ccv_status_string", "ccv_version", "ccv_fwd", "ccv_update",
-                          "paged_sconv_seq_metadata", "paged_sconv_fwd"}
+                          "ccv_update_spec", "paged_sconv_seq_metadata", "paged_sconv_fwd"}
     out = subprocess.run(["nm", "-D", "--defined-only", build.LIB], capture_output=True,
                          text=True, check=True).stdout
     exported = set(re.findall(r" T (\w+)$", out, flags=re.M))
@@ -100,6 +101,31 @@ def test_update_validation(lib):
     assert upd(lib, out=A + 2) == ALIAS  # overlapping but not identical to x
     assert upd(lib, batch=0) == OK
     assert upd(lib, seqlen=0) == OK
+
+
+def upd_spec(lib, **over):
+    args = dict(x=A, xsb=256, xsd=1, xst=64, out=A, osb=256, osd=1, ost=64, w=C, wsd=4, wsw=1,
+                bias=None, st=B, ssl=448, ssd=1, sst=64, nl=32, sl=7, idx=None, nacc=None,
+                inter=None, isb=0, ist=0, isd=0, isw=0, isteps=0, oidx=None, oisb=0, oist=0,
+                osteps=0, batch=4, dim=64, seqlen=4, width=4, pad=-1, silu=1, err=None,
+                stream=None)
+    args.update(over)
+    return lib.ccv_update_spec(*args.values())
+
+
+def test_update_spec_validation(lib):
+    assert upd_spec(lib, width=1) == WIDTH
+    assert upd_spec(lib, sl=5) == STATE                 # shifting needs W-2+seqlen = 6 columns
+    # with a buffer the line is not shifted, so W-1 columns suffice: 3 passes
+    # the column check and the capacity check decides; 2 fails it
+    assert upd_spec(lib, sl=3, oidx=D, oisb=4, oist=1, osteps=3) == CAP
+    assert upd_spec(lib, sl=2, oidx=D, oisb=4, oist=1, osteps=4) == STATE
+    assert upd_spec(lib, oidx=D, oisb=4, oist=1, osteps=3) == CAP
+    assert upd_spec(lib, inter=E, isb=768, ist=192, isd=1, isw=64, isteps=3) == CAP
+    assert upd_spec(lib, inter=E, isb=-1, ist=192, isd=1, isw=64, isteps=4) == STRIDE
+    assert upd_spec(lib, oidx=D, oisb=-4, oist=1, osteps=4) == STRIDE
+    assert upd_spec(lib, inter=B, isb=768, ist=192, isd=1, isw=64, isteps=4) == ALIAS
+    assert upd_spec(lib, batch=0) == OK
 
 
 def meta(lib, **over):
