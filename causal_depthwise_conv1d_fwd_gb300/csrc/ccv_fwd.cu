@@ -534,6 +534,15 @@ __global__ void __launch_bounds__(kCaThreads, 3) fwd_cl_async_kernel(const FwdAr
         if (active && j < nrows) cp_async16(ring_base + j * kCaThreads, src + j * xs);
         cp_async_commit();
     }
+    // The state line and the has_initial_state flag do not depend on each
+    // other: both loads go out with the stream, before the weights.
+    uint4 prior[W - 1];
+    bool init = false;
+    if (first && active && a.st != nullptr) {
+        init = a.has_init != nullptr && a.has_init[ci.seq] != 0;
+#pragma unroll
+        for (int j = 0; j < W - 1; ++j) prior[j] = load8_state(a, line, c0, j);
+    }
     stage_weights<W>(a.w, a.ws_d, a.ws_k, a.bias, a.dim, blockIdx.y * kCaTileC, kCaTileC, s_w, s_b);
     if (!active) return;
 
@@ -545,11 +554,9 @@ __global__ void __launch_bounds__(kCaThreads, 3) fwd_cl_async_kernel(const FwdAr
 
     uint4 ring[W - 1];
     if (first) {
-        uint4 prior[W - 1];
-        const bool init = a.st != nullptr && a.has_init != nullptr && a.has_init[ci.seq] != 0;
 #pragma unroll
         for (int j = 0; j < W - 1; ++j) {
-            prior[j] = init ? load8_state(a, line, c0, j) : make_uint4(0u, 0u, 0u, 0u);
+            if (!init) prior[j] = make_uint4(0u, 0u, 0u, 0u);
             ring[j] = prior[j];
         }
         if (a.st != nullptr) {
@@ -715,15 +722,19 @@ __global__ void __launch_bounds__(kCfaThreads, 4) fwd_cf_async_kernel(const FwdA
         cp_async_wait<0>();
         return;
     }
-    const bool init = chunk0 && a.st != nullptr && a.has_init != nullptr && a.has_init[ci.seq] != 0;
     uint32_t prior01 = 0, prior23 = 0;  // prior columns 0..3, packed
-    if (init) {
+    if (chunk0 && a.st != nullptr) {
+        // The flag and the state columns are loaded together (neither
+        // depends on the other); the columns count only when the flag is set.
+        const bool init = a.has_init != nullptr && a.has_init[ci.seq] != 0;
         const uint16_t *sp = a.st + line * a.ss_l + c * a.ss_d;
         uint32_t p[4] = {0, 0, 0, 0};
 #pragma unroll
         for (int j = 0; j < W - 1; ++j) p[j] = sp[j * a.ss_t];
-        prior01 = p[0] | (p[1] << 16);
-        prior23 = p[2] | (p[3] << 16);
+        if (init) {
+            prior01 = p[0] | (p[1] << 16);
+            prior23 = p[2] | (p[3] << 16);
+        }
     }
     auto issue_checked = [&](int seg) {
         if (seg >= nseg) return;
@@ -965,8 +976,9 @@ extern "C" int ccv_fwd(const void *x, int64_t x_stride_dim, int64_t x_stride_tok
     KernelFn fn = nullptr;
     dim3 grid;
     if (x_stride_dim == 1 && out_stride_dim == 1) {
-        const bool vec = dim % 8 == 0 && aligned16(x) && aligned16(out) &&
-                         x_stride_tok % 8 == 0 && out_stride_tok % 8 == 0;
+        // With a single token the token strides are never used.
+        const bool tok_ok = total_tokens <= 1 || (x_stride_tok % 8 == 0 && out_stride_tok % 8 == 0);
+        const bool vec = dim % 8 == 0 && aligned16(x) && aligned16(out) && tok_ok;
         a.st_vec = vec && conv_states != nullptr && s_stride_dim == 1 && aligned16(conv_states) &&
                    s_stride_line % 8 == 0 && s_stride_tok % 8 == 0;
         if (vec) return launch_cl_async(a, width, is_silu, stream);

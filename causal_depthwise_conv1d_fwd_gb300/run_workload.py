@@ -6,7 +6,8 @@ Used to give a profiler a small, self-contained program:
 
 Parts: prefill_tokens_dim, prefill_dim_tokens (4 x 4096 tokens, dim 8192),
 decode (256 x 8192), paged (H16 x ws128, 32 requests; metadata + conv),
-spec (speculative verify, 64 rows x 4 drafts, dim 8192).
+spec (speculative verify, 64 rows x 4 drafts, dim 8192), atrex (one
+channel-first sequence of --tokens x --dim, the atrex-bench #003 shapes).
 The process exits 0 after a device synchronize; it times nothing.
 """
 from __future__ import annotations
@@ -18,14 +19,14 @@ import torch
 from . import api
 from . import workloads as wl
 
-PARTS = ("prefill_tokens_dim", "prefill_dim_tokens", "decode", "paged", "spec")
+PARTS = ("prefill_tokens_dim", "prefill_dim_tokens", "decode", "paged", "spec", "atrex")
 
 
 def _dev(kwargs, dev):
     return {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in kwargs.items()}
 
 
-def make_launch(part: str, dev):
+def make_launch(part: str, dev, tokens: int = 1024, dim: int = 4096):
     if part.startswith("prefill"):
         layout = "tokens_dim" if part.endswith("tokens_dim") else "dim_tokens"
         d = _dev(wl.config_large_prefill(layout=layout).kwargs(), dev)
@@ -60,6 +61,12 @@ def make_launch(part: str, dev):
         d["intermediate_conv_window"] = inter
         launch = api.prepare_ccv_update_spec(**d)
         return lambda: launch()
+    if part == "atrex":
+        d = _dev(wl.config_atrex(tokens, dim).kwargs(), dev)
+        out = torch.empty_strided(d["x"].shape, d["x"].stride(), dtype=torch.bfloat16,
+                                  device=dev)
+        launch = api.prepare_ccv_fwd(**d, out=out)
+        return lambda: launch()
     raise ValueError(f"unknown part {part!r}; choose from {PARTS}")
 
 
@@ -67,10 +74,12 @@ def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--part", choices=PARTS, required=True)
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--tokens", type=int, default=1024, help="atrex part only")
+    ap.add_argument("--dim", type=int, default=4096, help="atrex part only")
     args = ap.parse_args(argv)
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    run = make_launch(args.part, dev)
+    run = make_launch(args.part, dev, args.tokens, args.dim)
     for _ in range(args.reps):
         run()
     torch.cuda.synchronize()

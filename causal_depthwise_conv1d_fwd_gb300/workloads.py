@@ -168,6 +168,20 @@ def config_single(seed: int = 1000) -> PrefillCase:
                           has_init="all", with_cache_indices=False, name="single_dim64_T16")
 
 
+# (tokens, dim) of the atrex-bench #003 "causal_conv1d" shape table.
+ATREX_SHAPES = ((1, 4096), (128, 4096), (256, 4096), (514, 4096), (1024, 4096),
+                (1, 8192), (4195, 8192), (11027, 8192), (14807, 8192))
+
+
+def config_atrex(tokens: int, dim: int, seed: int = 1006) -> PrefillCase:
+    """One channel-first sequence as in the atrex-bench #003 generator: x
+    (dim, tokens), weight (dim, 4), bias and initial state, all randn * 0.02,
+    SiLU on."""
+    return varlen_prefill(seed + tokens + dim, [tokens], dim, 4, num_cache_lines=1,
+                          layout="dim_tokens", has_init="all", with_cache_indices=False,
+                          name=f"atrex_T{tokens}_dim{dim}")
+
+
 def varlen_lengths(seed: int, batch: int = 8, lo: int = 1, hi: int = 512) -> List[int]:
     g = _gen(seed + 7919)
     return [int(v) for v in torch.randint(lo, hi + 1, (batch,), generator=g)]

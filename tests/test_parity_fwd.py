@@ -60,6 +60,13 @@ def test_config_large_prefill_full_size(layout):
     check(wl.config_large_prefill(layout=layout))
 
 
+@pytest.mark.parametrize("tokens,dim", wl.ATREX_SHAPES)
+def test_atrex_bench_shapes(tokens, dim):
+    """The nine shapes of the atrex-bench #003 table: one channel-first
+    sequence with initial state, bias and SiLU."""
+    check(wl.config_atrex(tokens, dim))
+
+
 # ------------------------------------------------------------- edge cases ----
 
 def _bf16_sweep(lo: float, hi: float) -> torch.Tensor:
