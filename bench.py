@@ -583,6 +583,51 @@ def atrex_shapes_timing(dev, calls=100):
     return rows
 
 
+def paged_streams_timing(dev, calls=100):
+    """A layer's four conv streams on one paged cache (not part of the step):
+    one fused launch vs one paged_sconv_fwd per stream, us per call L2-cold
+    (L2Flush between calls, outside the timed window), mean of many calls."""
+    import causal_depthwise_conv1d_fwd_gb300 as ccv
+    from causal_depthwise_conv1d_fwd_gb300 import workloads as wl
+
+    base, streams = wl.config_paged_streams()
+    cache = base.cache.to(dev)
+    meta = {k: getattr(base, k).to(dev) for k in
+            ("positions", "block_table", "seq_idx", "slot_mapping", "query_start")}
+    ds = [{"x": st["x"].to(dev), "weight": st["weight"].to(dev), "off_s": st["off_s"],
+           "ws": st["ws"]} for st in streams]
+    fused = ccv.prepare_paged_sconv_fwd_streams(ds, cache, block_size=base.block_size,
+                                                activation="silu", use_residual=True, **meta)
+    single = [ccv.prepare_paged_sconv_fwd(st["x"], st["weight"], cache, off_s=st["off_s"],
+                                          ws=st["ws"], block_size=base.block_size,
+                                          activation="silu", use_residual=True, **meta)
+              for st in ds]
+    stream = torch.cuda.current_stream().cuda_stream
+    flush = L2Flush(dev)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(calls)]
+        for a, b in evs:
+            flush()
+            a.record()
+            fn()
+            b.record()
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) * 1e3 for a, b in evs) / calls
+
+    us_fused = timed(lambda: fused(stream))
+    us_sep = timed(lambda: [launch(stream) for launch in single])
+    # every stream has the base case's channel count and token metadata
+    nbytes = len(streams) * _paged_bytes(base)
+    return {"workload": base.name, "kernel": "paged_vec_kernel", "streams": len(streams),
+            "bytes": nbytes, "us_fused_l2_cold": round(us_fused, 2),
+            "us_separate_l2_cold": round(us_sep, 2),
+            "gbs_fused": round(nbytes / (us_fused * 1e-6) / 1e9, 1)}
+
+
 def run_ours(args):
     import causal_depthwise_conv1d_fwd_gb300 as ccv  # noqa: F401
     from causal_depthwise_conv1d_fwd_gb300 import _lib
@@ -651,6 +696,7 @@ def run_ours(args):
     graph_us = decode_graph_us(dev_args)
     spec = spec_verify_timing(dev, rank)
     atrex = atrex_shapes_timing(dev)
+    paged_streams = paged_streams_timing(dev)
 
     if rank != 0:
         return
@@ -691,6 +737,7 @@ def run_ours(args):
         "decode_us_per_call_graph_warm": round(graph_us, 2),
         "spec_verify": spec,
         "atrex_shapes": atrex,
+        "paged_streams": paged_streams,
         "parts": parts_out,
         "roofline": {"bound": "hbm", "kernel": dominant.kernel, "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",

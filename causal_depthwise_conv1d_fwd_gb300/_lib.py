@@ -16,6 +16,13 @@ P = ctypes.c_void_p
 I64 = ctypes.c_int64
 I32 = ctypes.c_int
 
+class PagedStream(ctypes.Structure):
+    """struct ccv_paged_stream of include/ccv.h."""
+    _fields_ = [("x", P), ("x_stride_t", I64), ("weight", P), ("w_stride_c", I64),
+                ("w_stride_w", I64), ("out", P), ("out_stride_t", I64), ("off_s", I32),
+                ("ws", I32)]
+
+
 # Argument lists, in the order of the declarations in include/ccv.h.
 SIGNATURES = {
     "ccv_status_string": ([I32], ctypes.c_char_p),
@@ -34,6 +41,8 @@ SIGNATURES = {
     "paged_sconv_fwd": ([P, I64, P, I64, I64, I64, I32, I32, I32, I32,
                          P, I64, I64, P, I64, P, P, P, P, I64, I32, I32,
                          P, I32, I32, I32, I32, I32, I32, P, P], I32),
+    "paged_sconv_fwd_streams": ([P, I32, P, I64, I64, I64, I32, I32, I32, I32,
+                                 P, P, P, P, I64, I32, I32, P, I32, I32, I32, I32, P, P], I32),
 }
 
 _LIB = None

@@ -336,3 +336,70 @@ def prepare_paged_sconv_fwd(x, weight, cache, positions, block_table, seq_idx, s
             _silu_flag(activation), int(bool(use_residual)), _ptr(err_count))
     return Launch("paged_sconv_fwd", args, out,
                   (x, weight, cache, pos, sidx, slots, block_table, qs, out, err_count))
+
+
+def paged_sconv_fwd_streams(streams, cache: torch.Tensor, positions: torch.Tensor,
+                            block_table: torch.Tensor, seq_idx: torch.Tensor,
+                            slot_mapping: torch.Tensor, query_start: torch.Tensor,
+                            block_size: int, activation=None, use_residual: bool = True,
+                            err_count: Optional[torch.Tensor] = None, stream=None):
+    """paged_sconv_fwd for several conv streams of one layer in one launch.
+
+    streams: list of dicts with keys x, weight, off_s, ws and optionally out
+    (created when missing).  Returns the list of outputs."""
+    return prepare_paged_sconv_fwd_streams(streams, cache, positions, block_table, seq_idx,
+                                           slot_mapping, query_start, block_size, activation,
+                                           use_residual, err_count)(stream)
+
+
+def prepare_paged_sconv_fwd_streams(streams, cache, positions, block_table, seq_idx,
+                                    slot_mapping, query_start, block_size, activation=None,
+                                    use_residual=True, err_count=None) -> Launch:
+    """Validate and marshal a paged_sconv_fwd_streams call once."""
+    _need_cuda(cache, "cache", torch.bfloat16)
+    if cache.dim() != 4 or cache.stride(3) != 1:
+        raise ValueError("cache must be [num_blocks, H, N, D] with D stride 1")
+    num_blocks, H, N, D = cache.shape
+    if N != block_size:
+        raise ValueError("block_size does not match the cache's N")
+    if not 1 <= len(streams) <= 8:
+        raise ValueError("between 1 and 8 streams")
+    T = streams[0]["x"].shape[0]
+    width = streams[0]["weight"].shape[1]
+    descs = (_lib.PagedStream * len(streams))()
+    outs, keep = [], []
+    for i, st in enumerate(streams):
+        x, w, ws = st["x"], st["weight"], int(st["ws"])
+        _need_cuda(x, f"streams[{i}].x", torch.bfloat16)
+        _need_cuda(w, f"streams[{i}].weight", torch.bfloat16)
+        if x.dim() != 2 or x.stride(1) != 1 or x.shape[0] != T:
+            raise ValueError(f"streams[{i}].x must be [T, C] with channel stride 1")
+        if x.shape[1] != H * ws or w.dim() != 2 or w.shape[0] != H * ws or w.shape[1] != width:
+            raise ValueError(f"streams[{i}]: x / weight channels must equal H * ws, same width")
+        out = st.get("out")
+        if out is None:
+            out = torch.empty_like(x)
+        else:
+            _need_cuda(out, f"streams[{i}].out", torch.bfloat16)
+            if out.shape != x.shape or out.stride(1) != 1:
+                raise ValueError(f"streams[{i}].out must be [T, C] with channel stride 1")
+        descs[i] = _lib.PagedStream(x.data_ptr(), x.stride(0), w.data_ptr(), w.stride(0),
+                                    w.stride(1), out.data_ptr(), out.stride(0),
+                                    int(st["off_s"]), ws)
+        outs.append(out)
+        keep += [x, w, out]
+    pos = _index_vector(positions, "positions", torch.int64, T)
+    sidx = _index_vector(seq_idx, "seq_idx", torch.int32, T)
+    slots = _index_vector(slot_mapping, "slot_mapping", torch.int64, T)
+    qs = _index_vector(query_start, "query_start", torch.int32, T)
+    _need_cuda(block_table, "block_table", torch.int32)
+    if block_table.dim() != 2 or block_table.stride(1) != 1:
+        raise ValueError("block_table must be [num_reqs, max_blocks] with stride 1 along blocks")
+    _need_cuda(err_count, "err_count", torch.int32)
+    cs = cache.stride()
+    args = (ctypes.cast(descs, ctypes.c_void_p), len(streams), _ptr(cache), cs[0], cs[1], cs[2],
+            num_blocks, H, N, D, _ptr(pos), _ptr(sidx), _ptr(slots), _ptr(block_table),
+            block_table.stride(0), block_table.shape[0], block_table.shape[1], _ptr(qs), T,
+            width, _silu_flag(activation), int(bool(use_residual)), _ptr(err_count))
+    return Launch("paged_sconv_fwd_streams", args, outs,
+                  (descs, cache, pos, sidx, slots, block_table, qs, err_count, *keep))

@@ -54,6 +54,40 @@ struct PagedArgs {
     int *err;
 };
 
+// The fields that differ between the conv streams of one layer (each stream
+// owns its own x, weights, output and D-range of the shared cache).
+constexpr int kMaxStreams = 8;
+struct StreamFields {
+    const uint16_t *x;
+    int64_t xs_t;
+    const uint16_t *w;
+    int64_t ws_c, ws_k;
+    uint16_t *out;
+    int64_t os_t;
+    int off_s, ws, C, w_vec;
+};
+
+// One launch of the vector kernel: the shared arguments, and for a fused
+// multi-stream launch (gridDim.z > 1) the streams blockIdx.z selects.
+struct PagedLaunch {
+    PagedArgs a;
+    StreamFields s[kMaxStreams];
+};
+
+__host__ __device__ __forceinline__ void apply_stream(PagedArgs &a, const StreamFields &f) {
+    a.x = f.x;
+    a.xs_t = f.xs_t;
+    a.w = f.w;
+    a.ws_c = f.ws_c;
+    a.ws_k = f.ws_k;
+    a.out = f.out;
+    a.os_t = f.os_t;
+    a.off_s = f.off_s;
+    a.ws = f.ws;
+    a.C = f.C;
+    a.w_vec = f.w_vec;
+}
+
 // (block, offset) of a non-negative flat position in blocks of N.
 __device__ __forceinline__ void split_pos(const PagedArgs &a, int64_t p, int64_t &blk, int64_t &off) {
     if (a.n_shift >= 0) {
@@ -276,9 +310,24 @@ __device__ __forceinline__ uint4 paged_row(const uint4 (&wpk)[W], const uint4 (&
 }
 
 template <int W, bool SILU, bool RESID>
-__global__ void __launch_bounds__(kThreads, 7) paged_vec_kernel(const PagedArgs a) {
+__global__ void __launch_bounds__(kThreads, 7) paged_vec_kernel(const PagedLaunch pl) {
     extern __shared__ uint4 stage[];
     constexpr int R = kVecRun + W - 1;
+    PagedArgs a = pl.a;
+    if (gridDim.z > 1) {
+        // constant indices only: no dynamic indexing into the parameters
+        switch (blockIdx.z) {
+            case 0: apply_stream(a, pl.s[0]); break;
+            case 1: apply_stream(a, pl.s[1]); break;
+            case 2: apply_stream(a, pl.s[2]); break;
+            case 3: apply_stream(a, pl.s[3]); break;
+            case 4: apply_stream(a, pl.s[4]); break;
+            case 5: apply_stream(a, pl.s[5]); break;
+            case 6: apply_stream(a, pl.s[6]); break;
+            default: apply_stream(a, pl.s[7]); break;
+        }
+    }
+    if (blockIdx.y * kVecChannels >= a.C) return;  // this stream has fewer channel tiles
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int t0 = blockIdx.x * kVecBlockTokens + warp * kVecRun;
@@ -388,24 +437,37 @@ __global__ void __launch_bounds__(kThreads, 7) paged_vec_kernel(const PagedArgs 
     }
 }
 
-using PagedFn = void (*)(PagedArgs);
+using ScalarFn = void (*)(PagedArgs);
+using VecFn = void (*)(PagedLaunch);
 
 template <int W>
-PagedFn pick_w(bool vec, bool silu, bool resid) {
-    if (vec) {
-        if (silu) return resid ? paged_vec_kernel<W, true, true> : paged_vec_kernel<W, true, false>;
-        return resid ? paged_vec_kernel<W, false, true> : paged_vec_kernel<W, false, false>;
-    }
+VecFn pick_vec_w(bool silu, bool resid) {
+    if (silu) return resid ? paged_vec_kernel<W, true, true> : paged_vec_kernel<W, true, false>;
+    return resid ? paged_vec_kernel<W, false, true> : paged_vec_kernel<W, false, false>;
+}
+
+template <int W>
+ScalarFn pick_scalar_w(bool silu, bool resid) {
     if (silu) return resid ? paged_scalar_kernel<W, true, true> : paged_scalar_kernel<W, true, false>;
     return resid ? paged_scalar_kernel<W, false, true> : paged_scalar_kernel<W, false, false>;
 }
 
-PagedFn pick_kernel(int width, bool vec, bool silu, bool resid) {
+VecFn pick_vec(int width, bool silu, bool resid) {
     switch (width) {
-        case 2: return pick_w<2>(vec, silu, resid);
-        case 3: return pick_w<3>(vec, silu, resid);
-        case 4: return pick_w<4>(vec, silu, resid);
-        case 5: return pick_w<5>(vec, silu, resid);
+        case 2: return pick_vec_w<2>(silu, resid);
+        case 3: return pick_vec_w<3>(silu, resid);
+        case 4: return pick_vec_w<4>(silu, resid);
+        case 5: return pick_vec_w<5>(silu, resid);
+    }
+    return nullptr;
+}
+
+ScalarFn pick_scalar(int width, bool silu, bool resid) {
+    switch (width) {
+        case 2: return pick_scalar_w<2>(silu, resid);
+        case 3: return pick_scalar_w<3>(silu, resid);
+        case 4: return pick_scalar_w<4>(silu, resid);
+        case 5: return pick_scalar_w<5>(silu, resid);
     }
     return nullptr;
 }
@@ -466,6 +528,169 @@ extern "C" int paged_sconv_seq_metadata(const int32_t *query_start_loc, int num_
     return launch_status();
 }
 
+namespace ccv {
+namespace {
+
+// Shared arguments of every paged conv call (cache, token metadata, sizes).
+struct PagedShared {
+    void *cache;
+    int64_t cs_blk, cs_h, cs_n;
+    int num_blocks, H, N, D;
+    const int64_t *pos;
+    const int32_t *seq_idx;
+    const int64_t *slot;
+    const int32_t *bt;
+    int64_t bt_r;
+    int bt_rows, max_blocks;
+    const int32_t *qstart;
+    int T, width, silu, residual;
+    int *err;
+};
+
+int check_shared(const PagedShared &p) {
+    if (p.width < kMinWidth || p.width > kMaxWidth) return CCV_ERR_WIDTH;
+    if (p.T < 0 || p.num_blocks < 0 || p.H <= 0 || p.N <= 0 || p.D <= 0 || p.bt_rows < 0 ||
+        p.max_blocks <= 0)
+        return CCV_ERR_SIZE;
+    if (p.cs_blk < 0 || p.cs_h < 0 || p.cs_n < 0 || p.bt_r < 0) return CCV_ERR_STRIDE;
+    return CCV_OK;
+}
+
+int check_stream(const PagedShared &p, const ccv_paged_stream &st) {
+    if (st.ws <= 0) return CCV_ERR_SIZE;
+    if (st.off_s < 0 || st.off_s + st.ws > p.D) return CCV_ERR_RANGE;
+    if (st.x_stride_t < 0 || st.w_stride_c < 0 || st.w_stride_w < 0 || st.out_stride_t < 0)
+        return CCV_ERR_STRIDE;
+    if (static_cast<int64_t>(p.H) * st.ws > 0x7fffffffLL) return CCV_ERR_SIZE;
+    return CCV_OK;
+}
+
+Extent cache_extent(const PagedShared &p) {
+    const Extent ec = extent_of(p.cache, p.num_blocks > 0 ? p.num_blocks : 1, p.cs_blk, p.H,
+                                p.cs_h, p.N, p.cs_n);
+    return Extent{ec.lo, ec.hi + static_cast<uintptr_t>(p.D - 1) * 2u};
+}
+
+PagedArgs shared_args(const PagedShared &p) {
+    PagedArgs a{};
+    a.cache = static_cast<uint16_t *>(p.cache);
+    a.cs_blk = p.cs_blk;
+    a.cs_h = p.cs_h;
+    a.cs_n = p.cs_n;
+    a.num_blocks = p.num_blocks;
+    a.N = p.N;
+    a.pos = p.pos;
+    a.seq_idx = p.seq_idx;
+    a.slot = p.slot;
+    a.bt = p.bt;
+    a.bt_r = p.bt_r;
+    a.bt_rows = p.bt_rows;
+    a.max_blocks = p.max_blocks;
+    a.qstart = p.qstart;
+    a.T = p.T;
+    a.n_shift = (p.N & (p.N - 1)) == 0 ? __builtin_ctz(static_cast<unsigned>(p.N)) : -1;
+    a.err = p.err;
+    return a;
+}
+
+StreamFields stream_fields(const PagedShared &p, const ccv_paged_stream &st) {
+    StreamFields f;
+    f.x = static_cast<const uint16_t *>(st.x);
+    f.xs_t = st.x_stride_t;
+    f.w = static_cast<const uint16_t *>(st.weight);
+    f.ws_c = st.w_stride_c;
+    f.ws_k = st.w_stride_w;
+    f.out = static_cast<uint16_t *>(st.out);
+    f.os_t = st.out_stride_t;
+    f.off_s = st.off_s;
+    f.ws = st.ws;
+    f.C = p.H * st.ws;
+    f.w_vec = st.w_stride_w == 1 && st.w_stride_c == p.width && aligned16(st.weight);
+    return f;
+}
+
+// The 16-byte vector kernel applies: whole 8-channel vectors everywhere.
+bool vec_ok(const PagedShared &p, const ccv_paged_stream &st) {
+    return st.ws % 8 == 0 && st.off_s % 8 == 0 && aligned16(st.x) && aligned16(st.out) &&
+           aligned16(p.cache) && st.x_stride_t % 8 == 0 && st.out_stride_t % 8 == 0 &&
+           p.cs_blk % 8 == 0 && p.cs_h % 8 == 0 && p.cs_n % 8 == 0;
+}
+
+// Launch the given streams (all vector-capable) as one grid, blockIdx.z = stream.
+int launch_vec(const PagedShared &p, const ccv_paged_stream *streams, int n, ccv_stream_t stream) {
+    PagedLaunch pl;
+    pl.a = shared_args(p);
+    int max_c = 0;
+    for (int i = 0; i < kMaxStreams; ++i) pl.s[i] = stream_fields(p, streams[i < n ? i : 0]);
+    for (int i = 0; i < n; ++i) max_c = pl.s[i].C > max_c ? pl.s[i].C : max_c;
+    apply_stream(pl.a, pl.s[0]);
+    const dim3 grid(static_cast<unsigned>((p.T + kVecBlockTokens - 1) / kVecBlockTokens),
+                    static_cast<unsigned>((max_c + kVecChannels - 1) / kVecChannels),
+                    static_cast<unsigned>(n));
+    if (grid.y > 65535u) return CCV_ERR_SIZE;
+    pick_vec(p.width, p.silu != 0, p.residual != 0)<<<grid, kThreads, vec_smem(p.width), stream>>>(pl);
+    return launch_status();
+}
+
+int launch_scalar(const PagedShared &p, const ccv_paged_stream &st, ccv_stream_t stream) {
+    PagedArgs a = shared_args(p);
+    apply_stream(a, stream_fields(p, st));
+    const dim3 grid(static_cast<unsigned>((p.T + kBlockTokens - 1) / kBlockTokens),
+                    static_cast<unsigned>((a.C + 31) / 32));
+    if (grid.y > 65535u) return CCV_ERR_SIZE;
+    pick_scalar(p.width, p.silu != 0, p.residual != 0)<<<grid, kThreads, 0, stream>>>(a);
+    return launch_status();
+}
+
+int paged_run(const PagedShared &p, const ccv_paged_stream *streams, int n, ccv_stream_t stream) {
+    int rc = check_shared(p);
+    if (rc != CCV_OK) return rc;
+    if (n < 1 || n > kMaxStreams) return CCV_ERR_SIZE;
+    if (streams == nullptr) return CCV_ERR_NULL_POINTER;
+    for (int i = 0; i < n; ++i) {
+        rc = check_stream(p, streams[i]);
+        if (rc != CCV_OK) return rc;
+        for (int j = 0; j < i; ++j) {
+            // streams own disjoint D-ranges of the shared cache
+            const int lo = streams[i].off_s > streams[j].off_s ? streams[i].off_s : streams[j].off_s;
+            const int hi_i = streams[i].off_s + streams[i].ws, hi_j = streams[j].off_s + streams[j].ws;
+            if (lo < (hi_i < hi_j ? hi_i : hi_j)) return CCV_ERR_RANGE;
+        }
+    }
+    if (p.T == 0) return CCV_OK;
+    if (p.cache == nullptr || p.pos == nullptr || p.seq_idx == nullptr || p.slot == nullptr ||
+        p.bt == nullptr || p.qstart == nullptr)
+        return CCV_ERR_NULL_POINTER;
+    const Extent ec = cache_extent(p);
+    for (int i = 0; i < n; ++i) {
+        const ccv_paged_stream &st = streams[i];
+        if (st.x == nullptr || st.weight == nullptr || st.out == nullptr) return CCV_ERR_NULL_POINTER;
+        const int C = p.H * st.ws;
+        const Extent eo = extent_of(st.out, p.T, st.out_stride_t, C, 1);
+        if (overlaps(eo, ec)) return CCV_ERR_ALIAS;
+        for (int j = 0; j < n; ++j) {
+            const Extent ex = extent_of(streams[j].x, p.T, streams[j].x_stride_t, p.H * streams[j].ws, 1);
+            if (overlaps(eo, ex)) return CCV_ERR_ALIAS;
+            if (j < i && overlaps(eo, extent_of(streams[j].out, p.T, streams[j].out_stride_t,
+                                                p.H * streams[j].ws, 1)))
+                return CCV_ERR_ALIAS;
+        }
+    }
+    bool all_vec = true;
+    for (int i = 0; i < n; ++i) all_vec = all_vec && vec_ok(p, streams[i]);
+    if (all_vec) return launch_vec(p, streams, n, stream);
+    // Mixed layouts: each stream on its own, in order.
+    for (int i = 0; i < n; ++i) {
+        rc = vec_ok(p, streams[i]) ? launch_vec(p, streams + i, 1, stream)
+                                   : launch_scalar(p, streams[i], stream);
+        if (rc != CCV_OK) return rc;
+    }
+    return CCV_OK;
+}
+
+}  // namespace
+}  // namespace ccv
+
 extern "C" int paged_sconv_fwd(const void *x, int64_t x_stride_t, void *cache,
                                int64_t c_stride_blk, int64_t c_stride_h, int64_t c_stride_n,
                                int num_blocks, int H, int N, int D, const void *weight,
@@ -476,69 +701,24 @@ extern "C" int paged_sconv_fwd(const void *x, int64_t x_stride_t, void *cache,
                                int max_blocks, const int32_t *query_start, int T, int off_s,
                                int ws, int width, int silu, int residual, int *err_count,
                                ccv_stream_t stream) {
-    using namespace ccv;
-    if (width < kMinWidth || width > kMaxWidth) return CCV_ERR_WIDTH;
-    if (T < 0 || num_blocks < 0 || H <= 0 || N <= 0 || D <= 0 || ws <= 0 || bt_rows < 0 ||
-        max_blocks <= 0)
-        return CCV_ERR_SIZE;
-    if (off_s < 0 || off_s + ws > D) return CCV_ERR_RANGE;
-    if (x_stride_t < 0 || c_stride_blk < 0 || c_stride_h < 0 || c_stride_n < 0 ||
-        w_stride_c < 0 || w_stride_w < 0 || out_stride_t < 0 || bt_stride_r < 0)
-        return CCV_ERR_STRIDE;
-    const int64_t C64 = static_cast<int64_t>(H) * ws;
-    if (C64 > 0x7fffffffLL) return CCV_ERR_SIZE;
-    const int C = static_cast<int>(C64);
-    if (T == 0) return CCV_OK;
-    if (x == nullptr || cache == nullptr || weight == nullptr || out == nullptr ||
-        positions == nullptr || seq_idx == nullptr || slot_mapping == nullptr ||
-        block_table == nullptr || query_start == nullptr)
-        return CCV_ERR_NULL_POINTER;
-    const Extent ex = extent_of(x, T, x_stride_t, C, 1);
-    const Extent eo = extent_of(out, T, out_stride_t, C, 1);
-    const Extent ec = extent_of(cache, num_blocks > 0 ? num_blocks : 1, c_stride_blk, H,
-                                c_stride_h, N, c_stride_n);
-    const Extent ec_full{ec.lo, ec.hi + static_cast<uintptr_t>(D - 1) * 2u};
-    if (overlaps(ex, eo) || overlaps(eo, ec_full)) return CCV_ERR_ALIAS;
+    const ccv::PagedShared p{cache, c_stride_blk, c_stride_h, c_stride_n, num_blocks, H, N, D,
+                             positions, seq_idx, slot_mapping, block_table, bt_stride_r, bt_rows,
+                             max_blocks, query_start, T, width, silu, residual, err_count};
+    const ccv_paged_stream st{x, x_stride_t, weight, w_stride_c, w_stride_w, out, out_stride_t,
+                              off_s, ws};
+    return ccv::paged_run(p, &st, 1, stream);
+}
 
-    PagedArgs a;
-    a.x = static_cast<const uint16_t *>(x);
-    a.xs_t = x_stride_t;
-    a.cache = static_cast<uint16_t *>(cache);
-    a.cs_blk = c_stride_blk;
-    a.cs_h = c_stride_h;
-    a.cs_n = c_stride_n;
-    a.num_blocks = num_blocks;
-    a.N = N;
-    a.w = static_cast<const uint16_t *>(weight);
-    a.ws_c = w_stride_c;
-    a.ws_k = w_stride_w;
-    a.out = static_cast<uint16_t *>(out);
-    a.os_t = out_stride_t;
-    a.pos = positions;
-    a.seq_idx = seq_idx;
-    a.slot = slot_mapping;
-    a.bt = block_table;
-    a.bt_r = bt_stride_r;
-    a.bt_rows = bt_rows;
-    a.max_blocks = max_blocks;
-    a.qstart = query_start;
-    a.T = T;
-    a.off_s = off_s;
-    a.ws = ws;
-    a.C = C;
-    a.n_shift = (N & (N - 1)) == 0 ? __builtin_ctz(static_cast<unsigned>(N)) : -1;
-    a.w_vec = w_stride_w == 1 && w_stride_c == width && aligned16(weight);
-    a.err = err_count;
-
-    const bool vec = ws % 8 == 0 && off_s % 8 == 0 && aligned16(x) && aligned16(out) &&
-                     aligned16(cache) && x_stride_t % 8 == 0 && out_stride_t % 8 == 0 &&
-                     c_stride_blk % 8 == 0 && c_stride_h % 8 == 0 && c_stride_n % 8 == 0;
-    PagedFn fn = pick_kernel(width, vec, silu != 0, residual != 0);
-    const int block_tokens = vec ? kVecBlockTokens : kBlockTokens;
-    const int tile_c = vec ? kVecChannels : 32;
-    const dim3 grid(static_cast<unsigned>((T + block_tokens - 1) / block_tokens),
-                    static_cast<unsigned>((C + tile_c - 1) / tile_c));
-    if (grid.y > 65535u) return CCV_ERR_SIZE;
-    fn<<<grid, kThreads, vec ? vec_smem(width) : 0, stream>>>(a);
-    return launch_status();
+extern "C" int paged_sconv_fwd_streams(const ccv_paged_stream *streams, int num_streams,
+                                       void *cache, int64_t c_stride_blk, int64_t c_stride_h,
+                                       int64_t c_stride_n, int num_blocks, int H, int N, int D,
+                                       const int64_t *positions, const int32_t *seq_idx,
+                                       const int64_t *slot_mapping, const int32_t *block_table,
+                                       int64_t bt_stride_r, int bt_rows, int max_blocks,
+                                       const int32_t *query_start, int T, int width, int silu,
+                                       int residual, int *err_count, ccv_stream_t stream) {
+    const ccv::PagedShared p{cache, c_stride_blk, c_stride_h, c_stride_n, num_blocks, H, N, D,
+                             positions, seq_idx, slot_mapping, block_table, bt_stride_r, bt_rows,
+                             max_blocks, query_start, T, width, silu, residual, err_count};
+    return ccv::paged_run(p, streams, num_streams, stream);
 }

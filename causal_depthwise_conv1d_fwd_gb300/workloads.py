@@ -503,3 +503,40 @@ def config_paged(seed: int = 1004, num_blocks: int = 1024) -> PagedCase:
                  off_s=128, width=4, max_blocks=(2048 + 1024) // 16 + 8,
                  interior_pad_frac=interior, pad_rows=trailing, pad_multiple=8,
                  activation="silu", use_residual=True, name="paged_H16_ws128_32req")
+
+
+def paged_streams(base: PagedCase, seed: int, offsets, ws: int, std: float = STD):
+    """Conv streams sharing base's cache and token metadata: stream i owns
+    D-range [offsets[i], offsets[i] + ws).  Stream 0 reuses base's x and
+    weight; the others draw their own."""
+    g = _gen(seed)
+    T, C = base.x.shape
+    H = base.cache.shape[1]
+    if C != H * ws:
+        raise ValueError("base channels must equal H * ws")
+    streams = []
+    for i, off in enumerate(offsets):
+        if i == 0:
+            x, w = base.x, base.weight
+        else:
+            x = randn_bf16((T, C), g, std)
+            w = randn_bf16((C, base.weight.shape[1]), g, std)
+        streams.append({"x": x, "weight": w, "off_s": int(off), "ws": ws})
+    return streams
+
+
+def config_paged_streams(seed: int = 1007):
+    """A layer's four conv streams (K, V, attn-output, mlp-output): the paged
+    workload's requests and cache [1024, 16, 16, 512], each stream 128
+    channels per head at D offsets 0, 128, 256, 384.  Returns (base case,
+    streams)."""
+    lengths, starts = paged_mix(seed, num_blocks=1024)
+    T_actual = sum(lengths)
+    n_pad = max(2, int(round(0.02 * T_actual)))
+    trailing = n_pad // 2
+    base = paged(seed, lengths, starts, H=16, ws=128, N=16, D=512, num_blocks=1024, off_s=0,
+                 width=4, max_blocks=(2048 + 1024) // 16 + 8,
+                 interior_pad_frac=(n_pad - trailing) / max(T_actual, 1), pad_rows=trailing,
+                 pad_multiple=8, activation="silu", use_residual=True,
+                 name="paged_4streams_H16_ws128_32req")
+    return base, paged_streams(base, seed + 7, (0, 128, 256, 384), 128)

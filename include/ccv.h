@@ -228,6 +228,49 @@ int paged_sconv_fwd(const void *x, int64_t x_stride_t,
                     int width, int silu, int residual, int *err_count,
                     ccv_stream_t stream);
 
+/*
+ * One conv stream of a layer for paged_sconv_fwd_streams: its input, its
+ * weights, its output and the D-range [off_s, off_s + ws) of the shared
+ * cache it owns.  Fields mean what the same-named arguments of
+ * paged_sconv_fwd mean.
+ */
+typedef struct ccv_paged_stream {
+    const void *x;
+    int64_t x_stride_t;
+    const void *weight;
+    int64_t w_stride_c;
+    int64_t w_stride_w;
+    void *out;
+    int64_t out_stride_t;
+    int off_s;
+    int ws;
+} ccv_paged_stream;
+
+/*
+ * paged_sconv_fwd_streams -- paged_sconv_fwd for up to 8 conv streams of one
+ * layer in a single launch.  vLLM Inkling sconv.py, module docstring: a
+ * layer's streams (K, V, attn-output, mlp-output) share one paged cache,
+ * each in its own D-sub-range, and each is one `fused_sconv` call; the
+ * result equals calling paged_sconv_fwd once per stream, in any order.
+ *
+ * streams       HOST array of num_streams (1..8) descriptors, read during the
+ *               call only.  The streams' D-ranges must be pairwise disjoint
+ *               (CCV_ERR_RANGE otherwise); no out may overlap any x, another
+ *               out or the cache (CCV_ERR_ALIAS).
+ * Every other argument is shared by all streams and means what it means for
+ * paged_sconv_fwd (silu and residual apply to every stream).  When every
+ * stream allows 16-byte vectors one grid covers them all; otherwise each
+ * stream is launched on its own, in order, with the same results.
+ */
+int paged_sconv_fwd_streams(const ccv_paged_stream *streams, int num_streams,
+                            void *cache, int64_t c_stride_blk, int64_t c_stride_h,
+                            int64_t c_stride_n, int num_blocks, int H, int N, int D,
+                            const int64_t *positions, const int32_t *seq_idx,
+                            const int64_t *slot_mapping, const int32_t *block_table,
+                            int64_t bt_stride_r, int bt_rows, int max_blocks,
+                            const int32_t *query_start, int T, int width, int silu,
+                            int residual, int *err_count, ccv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -246,3 +246,20 @@ def paged_sconv_fwd(x, weight, cache, positions, block_table, seq_idx, slot_mapp
         _ptr(qs), T, off_s, ws, width,
         _silu_flag(activation), int(bool(use_residual)), ctypes.byref(err))
     return out, err.value
+
+
+def paged_sconv_fwd_streams(streams, cache, positions, block_table, seq_idx, slot_mapping,
+                            query_start, block_size, activation=None, use_residual=True):
+    """Several conv streams sharing one paged cache (vLLM Inkling sconv.py,
+    module docstring): each stream is one fused_sconv call on its own
+    D-range, so the definition is the single-stream routine applied to each
+    stream in turn.  streams: list of dicts with x, weight, off_s, ws.
+    Returns (list of outputs, total err_count); the cache is updated."""
+    outs, errs = [], 0
+    for st in streams:
+        out, err = paged_sconv_fwd(st["x"], st["weight"], cache, positions, block_table,
+                                   seq_idx, slot_mapping, query_start, st["off_s"], st["ws"],
+                                   block_size, activation, use_residual)
+        outs.append(out)
+        errs += err
+    return outs, errs

@@ -29,7 +29,8 @@ def lib():
 def test_every_declared_function_is_exported(lib):
     names = _lib.declared_functions()
     assert set(names) == {"ccv_status_string", "ccv_version", "ccv_fwd", "ccv_update",
-                          "ccv_update_spec", "paged_sconv_seq_metadata", "paged_sconv_fwd"}
+                          "ccv_update_spec", "paged_sconv_seq_metadata", "paged_sconv_fwd",
+                          "paged_sconv_fwd_streams"}
     out = subprocess.run(["nm", "-D", "--defined-only", build.LIB], capture_output=True,
                          text=True, check=True).stdout
     exported = set(re.findall(r" T (\w+)$", out, flags=re.M))
@@ -193,3 +194,30 @@ def test_product_path_does_not_touch_the_oracle():
                 text = open(os.path.join(root, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "ccv_oracle" not in text, f
+
+
+def streams_call(lib, descs, n=None, **over):
+    args = dict(streams=ctypes.cast(descs, ctypes.c_void_p) if descs is not None else None,
+                n=len(descs) if n is None else n, cache=B, csb=16 * 16 * 512, csh=16 * 512,
+                csn=512, nb=64, H=16, N=16, D=512, pos=C, seq=D, slot=E, bt=A, btr=8, btrows=4,
+                maxb=8, qs=A + 4096, T=32, width=4, silu=1, resid=1, err=None, stream=None)
+    args.update(over)
+    return lib.paged_sconv_fwd_streams(*args.values())
+
+
+def _descs(*ranges):
+    arr = (_lib.PagedStream * len(ranges))()
+    for i, (off, ws) in enumerate(ranges):
+        arr[i] = _lib.PagedStream(0x100000 * (i + 1), 16 * ws, 0x60000000 + 0x10000 * i, 4, 1,
+                                  0x70000000 + 0x100000 * i, 16 * ws, off, ws)
+    return arr
+
+
+def test_paged_streams_validation(lib):
+    assert streams_call(lib, _descs((0, 128), (64, 128))) == RANGE      # D-ranges overlap
+    assert streams_call(lib, _descs((0, 128), (448, 128))) == RANGE     # past D
+    assert streams_call(lib, _descs((0, 128)), n=0) == SIZE
+    assert streams_call(lib, _descs(*[(64 * i, 64) for i in range(8)]), n=9) == SIZE
+    assert streams_call(lib, None, n=2) == NULLP
+    assert streams_call(lib, _descs((0, 128), (128, 128)), width=6) == WIDTH
+    assert streams_call(lib, _descs((0, 128), (128, 128)), T=0) == OK

@@ -708,6 +708,34 @@ def test_paged_equals_prefill_with_cached_history():
         assert torch.equal(o.view(torch.int16), out[q[r]:q[r + 1]].t().view(torch.int16))
 
 
+def test_paged_streams_with_equal_inputs_agree_slice_by_slice():
+    """Streams that share inputs and histories but own different D-ranges
+    give identical outputs, and the cache is the initial cache with every real token's x
+    scattered into each stream's slice at its slot (nothing else changes)."""
+    base = _small_paged(460, [5, 1, 9], [0, 7, 3], D=40, off_s=0)
+    ws, N = base.ws, base.block_size
+    H = base.cache.shape[1]
+    offs = (0, ws, 3 * ws)
+    for off in offs[1:]:  # equal histories: every stream's slice starts as stream 0's
+        base.cache[..., off:off + ws] = base.cache[..., :ws]
+    streams = [{"x": base.x, "weight": base.weight, "off_s": off, "ws": ws} for off in offs]
+    cache = base.cache.clone()
+    outs, err = oracle.paged_sconv_fwd_streams(
+        streams, cache, base.positions, base.block_table, base.seq_idx, base.slot_mapping,
+        base.query_start, base.block_size, base.activation, base.use_residual)
+    assert err == 0
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+    expected = base.cache.clone()
+    for t in range(base.x.shape[0]):
+        slot = int(base.slot_mapping[t])
+        if slot < 0:
+            continue
+        for off in offs:
+            expected[slot // N, :, slot % N, off:off + ws] = base.x[t].view(H, ws)
+    assert torch.equal(cache.view(torch.int16), expected.view(torch.int16))
+
+
 def test_paged_invalid_block_is_counted():
     case = _small_paged(171, [2, 1], [5, 9])
     case.block_table[1, :] = 10_000
