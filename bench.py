@@ -628,6 +628,51 @@ def paged_streams_timing(dev, calls=100):
             "gbs_fused": round(nbytes / (us_fused * 1e-6) / 1e9, 1)}
 
 
+def width_variants_timing(dev, calls=20):
+    """The large prefill in both layouts for every width 2..5, with bias and
+    SiLU and without either (not part of the step).  Inputs are larger than
+    L2, so calls run back to back; us per call is the mean of many calls."""
+    import causal_depthwise_conv1d_fwd_gb300 as ccv
+    from causal_depthwise_conv1d_fwd_gb300 import workloads as wl
+
+    stream = torch.cuda.current_stream().cuda_stream
+    rows = []
+    for layout in ("tokens_dim", "dim_tokens"):
+        c = wl.config_large_prefill(layout=layout)
+        d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in c.kwargs().items()}
+        out = torch.empty_strided(d["x"].shape, d["x"].stride(), dtype=torch.bfloat16, device=dev)
+        g = torch.Generator().manual_seed(1008)
+        for width in (2, 3, 4, 5):
+            w = (torch.randn(c.dim, width, generator=g) * 0.02).to(torch.bfloat16).to(dev)
+            states = d["conv_states"]
+            if states.shape[2] < width - 1:  # W = 5 needs a fourth state column
+                states = wl.make_states(states.shape[0], c.dim, width - 1, "dim_contiguous",
+                                        g).to(dev)
+            for plain in (False, True):
+                dd = dict(d, weight=w, conv_states=states, bias=None if plain else d["bias"],
+                          activation=None if plain else "silu")
+                launch = ccv.prepare_ccv_fwd(**dd, out=out)
+                for _ in range(3):
+                    launch(stream)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                for _ in range(calls):
+                    launch(stream)
+                b.record()
+                torch.cuda.synchronize()
+                us = a.elapsed_time(b) * 1e3 / calls
+                case = wl.PrefillCase(c.name, c.x, torch.empty(c.dim, width, dtype=torch.bfloat16),
+                                      None if plain else c.bias, c.conv_states,
+                                      c.query_start_loc, c.cache_indices, c.has_initial_state,
+                                      None if plain else "silu", lengths=c.lengths)
+                nbytes = prefill_bytes(case)
+                rows.append({"layout": layout, "width": width,
+                             "bias_silu": not plain, "us": round(us, 2),
+                             "gbs": round(nbytes / (us * 1e-6) / 1e9, 1)})
+        del d, out
+    return rows
+
+
 def run_ours(args):
     import causal_depthwise_conv1d_fwd_gb300 as ccv  # noqa: F401
     from causal_depthwise_conv1d_fwd_gb300 import _lib
@@ -697,6 +742,7 @@ def run_ours(args):
     spec = spec_verify_timing(dev, rank)
     atrex = atrex_shapes_timing(dev)
     paged_streams = paged_streams_timing(dev)
+    widths = width_variants_timing(dev)
 
     if rank != 0:
         return
@@ -738,6 +784,7 @@ def run_ours(args):
         "spec_verify": spec,
         "atrex_shapes": atrex,
         "paged_streams": paged_streams,
+        "width_variants": widths,
         "parts": parts_out,
         "roofline": {"bound": "hbm", "kernel": dominant.kernel, "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",

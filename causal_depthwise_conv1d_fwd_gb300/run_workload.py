@@ -5,7 +5,7 @@ Used to give a profiler a small, self-contained program:
     python -m causal_depthwise_conv1d_fwd_gb300.run_workload --part prefill_tokens_dim --reps 3
 
 Parts: prefill_tokens_dim, prefill_dim_tokens (4 x 4096 tokens, dim 8192),
-decode (256 x 8192), paged (H16 x ws128, 32 requests; metadata + conv),
+decode (256 x 8192; prefill parts take --width), paged (H16 x ws128, 32 requests; metadata + conv),
 spec (speculative verify, 64 rows x 4 drafts, dim 8192), atrex (one
 channel-first sequence of --tokens x --dim, the atrex-bench #003 shapes).
 The process exits 0 after a device synchronize; it times nothing.
@@ -26,10 +26,17 @@ def _dev(kwargs, dev):
     return {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in kwargs.items()}
 
 
-def make_launch(part: str, dev, tokens: int = 1024, dim: int = 4096):
+def make_launch(part: str, dev, tokens: int = 1024, dim: int = 4096, width: int = 4):
     if part.startswith("prefill"):
         layout = "tokens_dim" if part.endswith("tokens_dim") else "dim_tokens"
-        d = _dev(wl.config_large_prefill(layout=layout).kwargs(), dev)
+        c = wl.config_large_prefill(layout=layout)
+        if width != 4:
+            g = torch.Generator().manual_seed(1008)
+            c.weight = (torch.randn(c.dim, width, generator=g) * 0.02).to(torch.bfloat16)
+            if c.conv_states.shape[2] < width - 1:
+                c.conv_states = wl.make_states(c.conv_states.shape[0], c.dim, width - 1,
+                                               "dim_contiguous", g)
+        d = _dev(c.kwargs(), dev)
         out = torch.empty_strided(d["x"].shape, d["x"].stride(), dtype=torch.bfloat16,
                                   device=dev)
         launch = api.prepare_ccv_fwd(**d, out=out)
@@ -76,10 +83,11 @@ def main(argv=None):
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--tokens", type=int, default=1024, help="atrex part only")
     ap.add_argument("--dim", type=int, default=4096, help="atrex part only")
+    ap.add_argument("--width", type=int, default=4, help="prefill parts only: conv width 2..5")
     args = ap.parse_args(argv)
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    run = make_launch(args.part, dev, args.tokens, args.dim)
+    run = make_launch(args.part, dev, args.tokens, args.dim, args.width)
     for _ in range(args.reps):
         run()
     torch.cuda.synchronize()
