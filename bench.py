@@ -390,7 +390,8 @@ def make_parts(dev, rank):
 
 def run_e2e(dev, cases, dev_args, steps):
     """The same step through the public API with host buffers: each step copies
-    its inputs from pinned host memory and reads its outputs back."""
+    its inputs from pinned host memory and reads its outputs back, pipelined
+    over a copy-in, a compute and a copy-out stream."""
     import causal_depthwise_conv1d_fwd_gb300 as ccv
 
     stream = torch.cuda.current_stream()
@@ -428,30 +429,84 @@ def run_e2e(dev, cases, dev_args, steps):
     h2d += hx.numel() * 2 + sum(v.numel() * v.element_size() for v in hmeta.values()) + hq.numel() * 4
     d2h += ho.numel() * 2
 
-    def one_step():
-        for name, d, out, hx, ho in plan:
-            d["x"].copy_(hx, non_blocking=True)
-            if name == "decode":
-                ccv.ccv_update(**d)
-            elif name == "paged":
-                for k, v in hmeta.items():
-                    d[k].copy_(v, non_blocking=True)
-                qsl_dev.copy_(hq, non_blocking=True)
-                ccv.paged_sconv_seq_metadata(qsl_dev, len(c.req_lengths), c.num_actual_tokens,
-                                             d["seq_idx"], d["query_start"], c.T)
-                ccv.paged_sconv_fwd(**d, out=out)
-            else:
-                ccv.ccv_fwd(**d, out=out)
-            ho.copy_(out, non_blocking=True)
+    # Copy-in streams, a compute stream and copy-out streams.  Part i's
+    # copy-in waits until the previous step's compute and copy-out of part i
+    # are done with its buffers; its compute waits for its copy-in and for the
+    # previous copy-out of its output; its copy-out waits for its compute.
+    # Copies in both directions and kernels of different parts overlap.
+    # KCOPY > 1 splits each copy over that many streams per direction; on
+    # GB300 that measured slower (the host link, not the copy engines, is the
+    # limit), so one stream per direction is used.
+    KCOPY = 1
+    s_in = [torch.cuda.Stream() for _ in range(KCOPY)]
+    s_out = [torch.cuda.Stream() for _ in range(KCOPY)]
+    s_comp = torch.cuda.Stream()
+    ev_in = [[torch.cuda.Event() for _ in range(KCOPY)] for _ in plan]
+    ev_out = [[torch.cuda.Event() for _ in range(KCOPY)] for _ in plan]
+    ev_done = [torch.cuda.Event() for _ in plan]
 
+    def flat(t):
+        # the host and device buffers share shape and strides and are dense,
+        # so their storage can be copied as flat element ranges
+        return t.as_strided((t.numel(),), (1,))
+
+    def pieces(n):
+        step = (n + KCOPY - 1) // KCOPY
+        return [(k * step, min(n, (k + 1) * step)) for k in range(KCOPY)]
+
+    def one_step():
+        for i, (name, d, out, hx, ho) in enumerate(plan):
+            src, dst = flat(hx), flat(d["x"])
+            for k, (lo, hi) in enumerate(pieces(src.numel())):
+                with torch.cuda.stream(s_in[k]):
+                    s_in[k].wait_event(ev_done[i])
+                    for e in ev_out[i]:
+                        s_in[k].wait_event(e)
+                    dst[lo:hi].copy_(src[lo:hi], non_blocking=True)
+                    if name == "paged" and k == 0:
+                        for key, v in hmeta.items():
+                            d[key].copy_(v, non_blocking=True)
+                        qsl_dev.copy_(hq, non_blocking=True)
+                    ev_in[i][k].record(s_in[k])
+            with torch.cuda.stream(s_comp):
+                for e in ev_in[i] + ev_out[i]:
+                    s_comp.wait_event(e)
+                if name == "decode":
+                    ccv.ccv_update(**d)
+                elif name == "paged":
+                    ccv.paged_sconv_seq_metadata(qsl_dev, len(c.req_lengths), c.num_actual_tokens,
+                                                 d["seq_idx"], d["query_start"], c.T)
+                    ccv.paged_sconv_fwd(**d, out=out)
+                else:
+                    ccv.ccv_fwd(**d, out=out)
+                ev_done[i].record(s_comp)
+            src, dst = flat(out), flat(ho)
+            for k, (lo, hi) in enumerate(pieces(src.numel())):
+                with torch.cuda.stream(s_out[k]):
+                    s_out[k].wait_event(ev_done[i])
+                    dst[lo:hi].copy_(src[lo:hi], non_blocking=True)
+                    ev_out[i][k].record(s_out[k])
+
+    all_streams = s_in + [s_comp] + s_out
+
+    def join():
+        for st in all_streams:
+            stream.wait_stream(st)
+
+    for st in all_streams:
+        st.wait_stream(stream)
     one_step()
+    join()
     torch.cuda.synchronize()
     barrier(dev)
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     start.record(stream)
+    for st in all_streams:
+        st.wait_stream(stream)
     for _ in range(steps):
         one_step()
+    join()
     end.record(stream)
     torch.cuda.synchronize()
     barrier(dev)
