@@ -513,20 +513,23 @@ def run_e2e(dev, cases, dev_args, steps):
     return start.elapsed_time(end) / 1e3, h2d, d2h
 
 
-def decode_graph_us(dev_args, replays=200):
-    """Warm (L2-resident) CUDA-graph replay of the decode call, us per call."""
-    import causal_depthwise_conv1d_fwd_gb300 as ccv
+GRAPH_CALLS = 20  # calls captured per graph, so replay measures the GPU, not the host launch
 
-    d, _ = dev_args["decode"]
+
+def graph_us_per_call(launch, replays=50):
+    """Warm (L2-resident) CUDA-graph replay: GRAPH_CALLS launches of `launch`
+    captured in one graph, us per call."""
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
-        ccv.ccv_update(**d)
+        launch(s.cuda_stream)
     torch.cuda.current_stream().wait_stream(s)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
-        ccv.ccv_update(**d)
-    for _ in range(10):
+        cs = torch.cuda.current_stream().cuda_stream
+        for _ in range(GRAPH_CALLS):
+            launch(cs)
+    for _ in range(5):
         g.replay()
     torch.cuda.synchronize()
     a = torch.cuda.Event(enable_timing=True)
@@ -536,7 +539,16 @@ def decode_graph_us(dev_args, replays=200):
         g.replay()
     b.record()
     torch.cuda.synchronize()
-    return a.elapsed_time(b) * 1e3 / replays
+    return a.elapsed_time(b) * 1e3 / (replays * GRAPH_CALLS)
+
+
+def decode_graph_us(dev_args):
+    """Warm CUDA-graph replay of the decode call, us per call."""
+    import causal_depthwise_conv1d_fwd_gb300 as ccv
+
+    d, _ = dev_args["decode"]
+    launch = ccv.prepare_ccv_update(**d)
+    return graph_us_per_call(lambda st: launch(st))
 
 
 class L2Flush:
@@ -583,26 +595,11 @@ def spec_verify_timing(dev, rank, calls=100):
     # mean, not median: single event pairs resolve only about 2 us here, and
     # the mean of many quantised readings is unbiased
     cold = sum(a.elapsed_time(b) * 1e3 for a, b in evs) / calls
-    s = torch.cuda.Stream()
-    s.wait_stream(stream)
-    with torch.cuda.stream(s):
-        launch(s.cuda_stream)
-    stream.wait_stream(s)
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        launch(torch.cuda.current_stream().cuda_stream)
-    for _ in range(10):
-        g.replay()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(200):
-        g.replay()
-    b.record()
-    torch.cuda.synchronize()
+    warm = graph_us_per_call(lambda st: launch(st))
     nbytes = spec_bytes(c)
     return {"workload": c.name, "kernel": "update_kernel", "bytes": nbytes,
             "us_l2_cold": round(cold, 2), "gbs_l2_cold": round(nbytes / (cold * 1e-6) / 1e9, 1),
-            "us_graph_warm": round(a.elapsed_time(b) * 1e3 / 200, 2)}
+            "us_graph_warm": round(warm, 2)}
 
 
 def atrex_shapes_timing(dev, calls=100):

@@ -25,6 +25,12 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Bring the line holding p into L1 (no register result, no wait).  Only for
+// data that no thread writes during the launch.
+__device__ __forceinline__ void prefetch_l1(const void *p) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
 // Wait until at most n of this thread's copy groups are pending (n <= 0:
 // all done; n >= 7: at most 7).  In a fully unrolled loop n folds to a
 // constant and only one wait instruction remains.

@@ -139,22 +139,9 @@ __device__ __forceinline__ uint4 decode_row(const uint4 (&wpk)[W], const float (
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// A block covers kThreads*VEC channels of kRows consecutive batch rows.  The
-// critical path is two dependent loads -- the rows' state-line indices, then
-// every row's state window and input at once -- with each thread's weights
-// loaded as 16-byte vectors while those loads are in flight.
-template <int W, bool SILU, int VEC>
-__global__ void __launch_bounds__(kThreads, VEC == 8 ? 7 : 1) update_kernel(const UpdArgs a) {
-    constexpr int TILE_C = kThreads * VEC;
-    __shared__ __align__(16) uint16_t s_w[W * TILE_C];
-    __shared__ __align__(16) uint16_t s_b[TILE_C];
-    const int rg = blockIdx.x / a.ctiles;
-    const int ct = blockIdx.x - rg * a.ctiles;
-    const int c0 = ct * TILE_C + threadIdx.x * VEC;
-    const bool active = c0 < a.dim;
-
-    // Resolve the rows' state lines (skipped rows get line -1).
-    int lines[kRows];
+// Resolve the rows' state lines (skipped rows get line -1).
+__device__ __forceinline__ void resolve_lines(const UpdArgs &a, int rg, bool active, int c0,
+                                              int (&lines)[kRows]) {
 #pragma unroll
     for (int r = 0; r < kRows; ++r) {
         const int b = rg * kRows + r;
@@ -170,54 +157,18 @@ __global__ void __launch_bounds__(kThreads, VEC == 8 ? 7 : 1) update_kernel(cons
         }
         lines[r] = line;
     }
+}
 
-    if (VEC == 8 && a.seqlen == 1 && a.plain) {
-        // Issue every row's window and input before anything else.
-        uint4 win[kRows][W - 1], xv[kRows];
-#pragma unroll
-        for (int r = 0; r < kRows; ++r) {
-            if (lines[r] < 0) continue;
-            const uint16_t *sp = a.st + lines[r] * a.ss_l + c0 * a.ss_d;
-#pragma unroll
-            for (int j = 0; j < W - 1; ++j) win[r][j] = gather<8>(sp + j * a.ss_t, a.ss_d, a.st_vec).v;
-            const int b = rg * kRows + r;
-            xv[r] = gather<8>(a.x + b * a.xs_b + c0 * a.xs_d, a.xs_d, a.x_vec).v;
-        }
-        if (!active) return;
-        uint4 wpk[W];
-        load_weights8<W>(a.w, a.ws_d, a.ws_k, c0, a.dim, a.w_vec, wpk);
-        float bs[8];
-        load_bias8(a.bias, c0, a.dim, a.b_vec, bs);
-#pragma unroll
-        for (int r = 0; r < kRows; ++r) {
-            if (lines[r] < 0) continue;
-            const int b = rg * kRows + r;
-            uint16_t *sp = a.st + lines[r] * a.ss_l + c0 * a.ss_d;
-            Raw<8> o;
-            o.v = decode_row<W, SILU>(wpk, bs, win[r], xv[r]);
-            scatter<8>(a.out + b * a.os_b + c0 * a.os_d, a.os_d, a.o_vec, o);
-            // The state keeps all but its oldest column and appends the input.
-#pragma unroll
-            for (int j = 0; j + 1 < W - 1; ++j) {
-                Raw<8> keep;
-                keep.v = win[r][j + 1];
-                scatter<8>(sp + j * a.ss_t, a.ss_d, a.st_vec, keep);
-            }
-            Raw<8> xin;
-            xin.v = xv[r];
-            scatter<8>(sp + (W - 2) * a.ss_t, a.ss_d, a.st_vec, xin);
-        }
-        return;
-    }
-
-    // General path: any seqlen, scalar or vector channels, fp32 arithmetic.
-    stage_weights<W>(a, ct * TILE_C, TILE_C, s_w, s_b);
-    if (!active) return;
+// General rows: any seqlen and the spec extras, fp32 arithmetic; the block's
+// weights and bias are staged as [tap][channel] (this thread's at s_w + k *
+// tile_c and s_b).
+template <int W, bool SILU, int VEC>
+__device__ __forceinline__ void general_rows(const UpdArgs &a, int rg, int c0, const int (&lines)[kRows],
+                                             const uint16_t *s_w, const uint16_t *s_b, int tile_c) {
     float wt[W][VEC], bs[VEC];
 #pragma unroll
-    for (int k = 0; k < W; ++k)
-        reinterpret_cast<const Raw<VEC> *>(s_w + k * TILE_C)[threadIdx.x].to_float(wt[k]);
-    reinterpret_cast<const Raw<VEC> *>(s_b)[threadIdx.x].to_float(bs);
+    for (int k = 0; k < W; ++k) reinterpret_cast<const Raw<VEC> *>(s_w + k * tile_c)->to_float(wt[k]);
+    reinterpret_cast<const Raw<VEC> *>(s_b)->to_float(bs);
     for (int r = 0; r < kRows; ++r) {
         if (lines[r] < 0) continue;
         const int b = rg * kRows + r;
@@ -279,6 +230,72 @@ __global__ void __launch_bounds__(kThreads, VEC == 8 ? 7 : 1) update_kernel(cons
                 }
             }
         }
+    }
+}
+
+// A block covers kThreads*VEC channels of kRows consecutive batch rows.
+// With 8-channel vectors this kernel only ever runs single-token rows without
+// the spec extras (the host sends everything else to spec_kernel): weights
+// and bias are requested first, overlapping the round trip for the rows'
+// state-line indices, then every row's state window and input, then the
+// mixed-precision taps.  With one channel per thread it is the general
+// path: any seqlen, the spec extras, fp32 arithmetic.
+template <int W, bool SILU, int VEC>
+__global__ void __launch_bounds__(kThreads, VEC == 8 ? 7 : 1) update_kernel(const UpdArgs a) {
+    constexpr int TILE_C = kThreads * VEC;
+    const int rg = blockIdx.x / a.ctiles;
+    const int ct = blockIdx.x - rg * a.ctiles;
+    const int c0 = ct * TILE_C + threadIdx.x * VEC;
+    const bool active = c0 < a.dim;
+
+    if constexpr (VEC == 8) {
+        uint4 wpk[W];
+        float bs[8];
+        if (active) {
+            load_weights8<W>(a.w, a.ws_d, a.ws_k, c0, a.dim, a.w_vec, wpk);
+            load_bias8(a.bias, c0, a.dim, a.b_vec, bs);
+        }
+        int lines[kRows];
+        resolve_lines(a, rg, active, c0, lines);
+        uint4 win[kRows][W - 1], xv[kRows];
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) {
+            if (lines[r] < 0) continue;
+            const uint16_t *sp = a.st + lines[r] * a.ss_l + c0 * a.ss_d;
+#pragma unroll
+            for (int j = 0; j < W - 1; ++j) win[r][j] = gather<8>(sp + j * a.ss_t, a.ss_d, a.st_vec).v;
+            const int b = rg * kRows + r;
+            xv[r] = gather<8>(a.x + b * a.xs_b + c0 * a.xs_d, a.xs_d, a.x_vec).v;
+        }
+        if (!active) return;
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) {
+            if (lines[r] < 0) continue;
+            const int b = rg * kRows + r;
+            uint16_t *sp = a.st + lines[r] * a.ss_l + c0 * a.ss_d;
+            Raw<8> o;
+            o.v = decode_row<W, SILU>(wpk, bs, win[r], xv[r]);
+            scatter<8>(a.out + b * a.os_b + c0 * a.os_d, a.os_d, a.o_vec, o);
+            // The state keeps all but its oldest column and appends the input.
+#pragma unroll
+            for (int j = 0; j + 1 < W - 1; ++j) {
+                Raw<8> keep;
+                keep.v = win[r][j + 1];
+                scatter<8>(sp + j * a.ss_t, a.ss_d, a.st_vec, keep);
+            }
+            Raw<8> xin;
+            xin.v = xv[r];
+            scatter<8>(sp + (W - 2) * a.ss_t, a.ss_d, a.st_vec, xin);
+        }
+    } else {
+        __shared__ __align__(16) uint16_t s_w[W * TILE_C];
+        __shared__ __align__(16) uint16_t s_b[TILE_C];
+        int lines[kRows];
+        resolve_lines(a, rg, active, c0, lines);
+        stage_weights<W>(a, ct * TILE_C, TILE_C, s_w, s_b);
+        if (!active) return;
+        general_rows<W, SILU, VEC>(a, rg, c0, lines, s_w + threadIdx.x * VEC, s_b + threadIdx.x * VEC,
+                                   TILE_C);
     }
 }
 

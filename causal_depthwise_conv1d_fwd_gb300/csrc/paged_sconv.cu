@@ -391,6 +391,19 @@ __global__ void __launch_bounds__(kThreads, 7) paged_vec_kernel(const PagedLaunc
     // any of the group's stores, so their latencies overlap instead of
     // queueing behind the stores (which the compiler cannot prove disjoint).
     constexpr int kGroup = W <= 3 ? 4 : 2;  // at most 8 vectors of taps in flight
+    // First pull every cache tap of the run into L1: prefetches hold no
+    // registers, so the whole run's round trip overlaps, and the grouped
+    // loads below hit L1.  Pre-forward positions are never written in this
+    // launch, so their lines in L1 stay valid.
+#pragma unroll 1
+    for (int u = 0; u < n; ++u) {
+        const int kinds = __shfl_sync(kFullMask, mine.kinds, u);
+#pragma unroll
+        for (int iw = 0; iw < W; ++iw) {
+            const int64_t off = shfl64(mine.off[iw], u);
+            if (active && ((kinds >> (2 * iw)) & 3) == kTapCache) prefetch_l1(a.cache + off + chan_off);
+        }
+    }
     cp_async_wait<0>();
 #pragma unroll 1
     for (int g = 0; g < n; g += kGroup) {
