@@ -278,6 +278,7 @@ KERNEL_SOURCE = {
     "fwd_cl_async_kernel": "ccv_fwd.cu",
     "fwd_cf_async_kernel": "ccv_fwd.cu",
     "update_kernel": "ccv_update.cu",
+    "spec_kernel": "ccv_update.cu",
     "paged_vec_kernel": "paged_sconv.cu",
     "seq_metadata_kernel": "paged_sconv.cu",
 }
@@ -597,7 +598,7 @@ def spec_verify_timing(dev, rank, calls=100):
     cold = sum(a.elapsed_time(b) * 1e3 for a, b in evs) / calls
     warm = graph_us_per_call(lambda st: launch(st))
     nbytes = spec_bytes(c)
-    return {"workload": c.name, "kernel": "update_kernel", "bytes": nbytes,
+    return {"workload": c.name, "kernel": "spec_kernel", "bytes": nbytes,
             "us_l2_cold": round(cold, 2), "gbs_l2_cold": round(nbytes / (cold * 1e-6) / 1e9, 1),
             "us_graph_warm": round(warm, 2)}
 
