@@ -824,9 +824,9 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "width": 4, "dim": 8192,
+        "config": {"workload": WORKLOAD, "width": 4, "dim": 8192, "storage": "bf16",
                    "prefill_tokens": sum(p.tokens for p in pre) // 2,
                    "bytes_per_step": step_bytes,
                    "l2": "inputs larger than L2: each step streams 1.07 GB of prefill traffic, "
@@ -976,8 +976,8 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ts * 1e3 / args.steps, 3), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "width": 4, "dim": 8192,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "width": 4, "dim": 8192, "storage": "bf16",
                    "sample": f"{frac:.5f} of the channels of every part per step"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": f"{frac:.5f} of the channels of every part per step, "
