@@ -10,8 +10,9 @@ extern "C" const char *ccv_status_string(int status) {
         case CCV_ERR_STATE_LEN: return "conv_state has fewer columns than the method needs";
         case CCV_ERR_ALIAS: return "an output overlaps an input it may not alias";
         case CCV_ERR_STRIDE: return "a stride is negative";
-        case CCV_ERR_RANGE: return "the stream slice [off_s, off_s+ws) leaves the cache's D range";
-        case CCV_ERR_CAPACITY: return "an output buffer is smaller than the padded token count";
+        case CCV_ERR_RANGE:
+            return "a stream's D-range [off_s, off_s+ws) leaves the cache or overlaps another stream's";
+        case CCV_ERR_CAPACITY: return "an output buffer has fewer entries than the call needs";
         case CCV_ERR_ARGUMENT: return "has_initial_state needs conv_states";
         default: break;
     }
@@ -19,4 +20,5 @@ extern "C" const char *ccv_status_string(int status) {
     return "unknown ccv status";
 }
 
-extern "C" int ccv_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+// 1.1.0: ccv_update_spec and paged_sconv_fwd_streams added.
+extern "C" int ccv_version(void) { return 1 * 10000 + 1 * 100 + 0; }

@@ -50,8 +50,8 @@ enum ccv_status {
     CCV_ERR_STATE_LEN = -4,     /* state storage narrower than the method needs */
     CCV_ERR_ALIAS = -5,         /* out overlaps x where that is not allowed */
     CCV_ERR_STRIDE = -6,        /* a stride the method requires to be 1 is not */
-    CCV_ERR_RANGE = -7,         /* stream slice / offsets outside the cache */
-    CCV_ERR_CAPACITY = -8,      /* output buffer smaller than the padded count */
+    CCV_ERR_RANGE = -7,         /* stream D-range outside the cache or overlapping another */
+    CCV_ERR_CAPACITY = -8,      /* an output buffer has fewer entries than needed */
     CCV_ERR_ARGUMENT = -9       /* an argument combination the pages reject */
 };
 
