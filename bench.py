@@ -285,15 +285,16 @@ KERNEL_SOURCE = {
 
 
 def kernel_sources_sha(kernel: str) -> str:
-    """Hash of the sources `kernel` is built from: its own .cu file, the
-    shared device headers and the C header."""
+    """Hash of the sources `kernel` is built from: its own .cu file and the
+    shared device headers (the C header declares the ABI; no device code
+    depends on it)."""
     from causal_depthwise_conv1d_fwd_gb300 import build as lib_build
 
     own = KERNEL_SOURCE[kernel]
     h = hashlib.sha256()
     for f in sorted(lib_build._inputs()):
         name = os.path.basename(f)
-        if f.endswith(".cu") and name != own:
+        if not (name == own or name.endswith(".cuh")):
             continue
         with open(f, "rb") as fh:
             h.update(name.encode())
