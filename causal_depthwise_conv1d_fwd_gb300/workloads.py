@@ -295,11 +295,12 @@ def spec_decode(seed: int, batch: int, dim: int, width: int = 4, seqlen: int = 4
     The intermediate buffer starts as random values, so untouched entries are
     recognisable."""
     g = _gen(seed)
-    num_lines = 3 * batch * max(1, seqlen) if num_lines is None else num_lines
+    steps = seqlen if steps is None else steps
+    if num_lines is None:  # room for the input lines and distinct output lines
+        num_lines = max(3 * batch * max(1, seqlen), batch * (steps + 3))
     state_len = width - 1 + history
     if not (with_intermediate or with_output_indices):
         state_len = max(state_len, width - 2 + seqlen)
-    steps = seqlen if steps is None else steps
     # channels contiguous (x.stride(1) == 1), the layout the page's update
     # wrapper asserts
     x = randn_bf16((batch, seqlen, dim), g, std).transpose(1, 2)
@@ -334,7 +335,7 @@ def config_spec_decode(seed: int = 1005) -> SpecDecodeCase:
     """Speculative verify: 64 rows x 4 draft tokens, dim 8192, W 4, history of
     4 columns, num_accepted_tokens in [1, 5], per-step windows written to an
     intermediate buffer and scattered to output state lines."""
-    return spec_decode(seed, 64, 8192, 4, 4, history=4, with_accepted=True,
+    return spec_decode(seed, 64, 8192, 4, 4, num_lines=768, history=4, with_accepted=True,
                        with_intermediate=True, with_output_indices=True,
                        name="spec_verify_64x4_dim8192")
 
