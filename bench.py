@@ -727,6 +727,38 @@ def width_variants_timing(dev, calls=20):
     return rows
 
 
+def small_configs_timing(dev, calls=100):
+    """The single-sequence (dim 64, 16 tokens) and varlen continuous-batching
+    (8 sequences, dim 4096) prefill configurations, not part of the step: us
+    per call L2-cold (L2Flush between calls, outside the timed window), mean
+    of many calls."""
+    import causal_depthwise_conv1d_fwd_gb300 as ccv
+    from causal_depthwise_conv1d_fwd_gb300 import workloads as wl
+
+    stream = torch.cuda.current_stream().cuda_stream
+    flush = L2Flush(dev)
+    rows = []
+    for c in (wl.config_single(), wl.config_varlen()):
+        d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in c.kwargs().items()}
+        out = torch.empty_strided(d["x"].shape, d["x"].stride(), dtype=torch.bfloat16, device=dev)
+        launch = ccv.prepare_ccv_fwd(**d, out=out)
+        for _ in range(3):
+            launch(stream)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(calls)]
+        for a, b in evs:
+            flush()
+            a.record()
+            launch(stream)
+            b.record()
+        torch.cuda.synchronize()
+        us = sum(a.elapsed_time(b) * 1e3 for a, b in evs) / calls
+        nbytes = prefill_bytes(c)
+        rows.append({"workload": c.name, "tokens": prefill_tokens(c), "us_l2_cold": round(us, 2),
+                     "gbs": round(nbytes / (us * 1e-6) / 1e9, 1), "bytes": nbytes})
+    return rows
+
+
 def run_ours(args):
     import causal_depthwise_conv1d_fwd_gb300 as ccv  # noqa: F401
     from causal_depthwise_conv1d_fwd_gb300 import _lib
@@ -797,6 +829,7 @@ def run_ours(args):
     atrex = atrex_shapes_timing(dev)
     paged_streams = paged_streams_timing(dev)
     widths = width_variants_timing(dev)
+    small = small_configs_timing(dev)
 
     if rank != 0:
         return
@@ -840,6 +873,7 @@ def run_ours(args):
         "atrex_shapes": atrex,
         "paged_streams": paged_streams,
         "width_variants": widths,
+        "small_configs": small,
         "parts": parts_out,
         "roofline": {"bound": "hbm", "kernel": dominant.kernel, "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
