@@ -9,11 +9,17 @@
 // intermediate buffer and/or scattered to an output state line, and no
 // in-place shift when either of those is requested.
 //
-// One thread owns 8 consecutive channels (16-byte vectors) of kRows
-// consecutive batch rows; the grid is ceil(batch / kRows) x ceil(dim / 1024)
-// blocks, fixed by the sizes, so a CUDA graph replays it unchanged.  Every element of the state line and of out is
-// read and written by the same thread, which makes the in-place state shift
-// and out == x (the page's wrapper writes the output over x) hazard-free.
+// Three kernels, picked on the host from the sizes alone (so a CUDA graph
+// replays the same launch):
+//   * update_kernel<.., 8>: single-token rows without the spec extras; a
+//     thread owns 8 consecutive channels (16-byte vectors) of kRows rows;
+//   * spec_kernel: several tokens per row or any spec extra, 8 channels and
+//     one row per thread;
+//   * update_kernel<.., 1>: everything else (dims that are not a multiple of
+//     8), one channel per thread.
+// Every element of a state line and of out is read and written by the same
+// thread, which makes the in-place state shift and out == x (the page's
+// wrapper writes the output over x) hazard-free.
 #include "ccv_common.cuh"
 #include "ccv_math2.cuh"
 
