@@ -620,8 +620,9 @@ __global__ void __launch_bounds__(kCaThreads, W == 5 ? 2 : 3) fwd_cl_async_kerne
 // vector that crosses the chunk's edge is assembled with scalar loads, the
 // prior included, and stored into the slot instead).  The 4 tokens before a
 // lane's vector come from lane l-1 by shuffle (lane 0: lane 31 of the
-// previous segment).  Taps are scalar fp32 FMAs on the widened 12-token
-// window; segments wholly inside the chunk run without per-lane checks.
+// previous segment).  Taps are native bf16 x bf16 + fp32 FMAs on the packed
+// 12-token window; segments wholly inside the chunk run without per-lane
+// checks.
 
 constexpr int kCfaThreads = 256;
 constexpr int kCfaWarps = kCfaThreads / 32;
