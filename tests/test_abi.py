@@ -7,6 +7,8 @@ call here is built to fail validation or to be empty work.
 from __future__ import annotations
 
 import ctypes
+import os
+import sys
 import re
 import subprocess
 
@@ -221,3 +223,21 @@ def test_paged_streams_validation(lib):
     assert streams_call(lib, None, n=2) == NULLP
     assert streams_call(lib, _descs((0, 128), (128, 128)), width=6) == WIDTH
     assert streams_call(lib, _descs((0, 128), (128, 128)), T=0) == OK
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """Without libccv.so the binding raises; it never falls back to another path."""
+    code = (
+        "import causal_depthwise_conv1d_fwd_gb300._lib as L\n"
+        f"L.LIB_PATH = {str(tmp_path / 'absent.so')!r}\n"
+        "L._LIB = None\n"
+        "try:\n"
+        "    L.load()\n"
+        "except RuntimeError as e:\n"
+        "    print('raised:', e)\n"
+        "else:\n"
+        "    raise SystemExit('no error')\n")
+    proc = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True,
+                          cwd=os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    assert proc.returncode == 0, proc.stderr
+    assert "not built" in proc.stdout
