@@ -116,3 +116,73 @@ def test_paged_random(seed):
     torch.cuda.synchronize()
     assert_close(out, ref_out, case.name)
     assert_bits(d["cache"], ref_cache, f"{case.name} cache")
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_paged_streams_random(seed):
+    r = random.Random(7300 + seed)
+    width = r.randint(2, 5)
+    H = r.choice([1, 2, 4])
+    N = r.choice([8, 16])
+    nreq = r.randint(1, 5)
+    lengths = [r.choice([1, 1, 4, r.randint(2, 50)]) for _ in range(nreq)]
+    starts = [r.choice([0, 2, r.randint(0, 100)]) for _ in range(nreq)]
+    # disjoint D-ranges of random widths, in a random order
+    widths = [r.choice([8, 16, 24, 12]) for _ in range(r.randint(1, 4))]
+    offs, pos = [], 0
+    for w in widths:
+        pos += r.choice([0, 8])
+        offs.append(pos)
+        pos += w
+    D = pos + r.choice([0, 8])
+    order = list(range(len(widths)))
+    r.shuffle(order)
+    base = wl.paged(8300 + seed, lengths, starts, H=H, ws=widths[0], N=N, D=D, num_blocks=128,
+                    off_s=offs[0], width=width, interior_pad_frac=r.choice([0.0, 0.1]),
+                    pad_rows=r.choice([0, 2]), pad_multiple=8,
+                    activation=r.choice(["silu", None]), use_residual=r.random() < 0.6,
+                    name=f"fuzz_streams_{seed}")
+    g = torch.Generator().manual_seed(8400 + seed)
+    T = base.x.shape[0]
+    streams = []
+    for i in order:
+        ws = widths[i]
+        x = base.x if i == 0 else (torch.randn(T, H * ws, generator=g) * 0.02).to(torch.bfloat16)
+        w = (base.weight if i == 0 else
+             (torch.randn(H * ws, width, generator=g) * 0.02).to(torch.bfloat16))
+        streams.append({"x": x, "weight": w, "off_s": offs[i], "ws": ws})
+    ref_cache = base.cache.clone()
+    ref_outs, _ = oracle.paged_sconv_fwd_streams(
+        streams, ref_cache, base.positions, base.block_table, base.seq_idx, base.slot_mapping,
+        base.query_start, base.block_size, base.activation, base.use_residual)
+    cache = base.cache.to(DEV)
+    meta = {k: getattr(base, k).to(DEV) for k in
+            ("positions", "block_table", "seq_idx", "slot_mapping", "query_start")}
+    outs = ccv.paged_sconv_fwd_streams(
+        [{"x": st["x"].to(DEV), "weight": st["weight"].to(DEV), "off_s": st["off_s"],
+          "ws": st["ws"]} for st in streams], cache, block_size=base.block_size,
+        activation=base.activation, use_residual=base.use_residual, **meta)
+    torch.cuda.synchronize()
+    for i, (o, ref) in enumerate(zip(outs, ref_outs)):
+        assert_close(o, ref, f"{base.name} stream {i}")
+    assert_bits(cache, ref_cache, f"{base.name} cache")
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_metadata_random(seed):
+    r = random.Random(7400 + seed)
+    num_reqs = r.randint(1, 40)
+    lengths = [r.choice([0, 1, 1, 4, r.randint(1, 300)]) for _ in range(num_reqs)]
+    qsl = torch.tensor([0] + list(torch.tensor(lengths).cumsum(0)), dtype=torch.int32)
+    actual = int(qsl[-1])
+    padded = actual + r.choice([0, 1, 7, 64])
+    cap = padded + r.choice([0, 5])
+    ref_seq = torch.full((cap,), 77, dtype=torch.int32)
+    ref_qs = ref_seq.clone()
+    oracle.paged_sconv_seq_metadata(qsl, num_reqs, actual, ref_seq, ref_qs, padded)
+    seq = torch.full((cap,), 77, dtype=torch.int32, device=DEV)
+    qs = seq.clone()
+    ccv.paged_sconv_seq_metadata(qsl.to(DEV), num_reqs, actual, seq, qs, padded)
+    torch.cuda.synchronize()
+    assert_bits(seq.cpu(), ref_seq, "seq_idx")
+    assert_bits(qs.cpu(), ref_qs, "query_start")
