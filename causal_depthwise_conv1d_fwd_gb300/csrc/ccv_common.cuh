@@ -1,6 +1,8 @@
 // Shared device and host helpers of the ccv CUDA library (sm_103a).
 #pragma once
 
+#include <atomic>
+
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -200,8 +202,10 @@ inline bool overlaps(const Extent &a, const Extent &b) { return a.lo <= b.hi && 
 constexpr int kMaxDevices = 64;
 
 // Streaming multiprocessors of the current device (cached per device).
+// The caches below may be filled by several host threads at once; every
+// writer stores the same value, and relaxed atomics make that well defined.
 inline int current_device_sms(int *device_out = nullptr) {
-    static int cache[kMaxDevices] = {0};
+    static std::atomic<int> cache[kMaxDevices];  // zero-initialised (static storage)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
     if (device_out) *device_out = dev;
@@ -210,12 +214,14 @@ inline int current_device_sms(int *device_out = nullptr) {
         cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
         return n > 0 ? n : 1;
     }
-    if (cache[dev] == 0) {
+    int cached = cache[dev].load(std::memory_order_relaxed);
+    if (cached == 0) {
         int n = 0;
         cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        cache[dev] = n > 0 ? n : 1;
+        cached = n > 0 ? n : 1;
+        cache[dev].store(cached, std::memory_order_relaxed);
     }
-    return cache[dev];
+    return cached;
 }
 
 // Prepare `fn` to run with `threads` threads and `bytes` of dynamic shared
@@ -225,11 +231,14 @@ inline int current_device_sms(int *device_out = nullptr) {
 // ones made while a CUDA graph is being captured -- only read the cache.
 template <auto kKernel>
 inline int resident_blocks(int threads, size_t bytes, int dev, cudaError_t *err) {
-    static int cache[kMaxDevices] = {0};  // one cache per kernel instantiation
+    static std::atomic<int> cache[kMaxDevices];  // one cache per kernel instantiation
     const auto fn = kKernel;
     *err = cudaSuccess;
     const bool cacheable = dev >= 0 && dev < kMaxDevices;
-    if (cacheable && cache[dev] > 0) return cache[dev];
+    if (cacheable) {
+        const int cached = cache[dev].load(std::memory_order_relaxed);
+        if (cached > 0) return cached;
+    }
     cudaError_t e =
         cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
     int blocks = 0;
@@ -238,7 +247,7 @@ inline int resident_blocks(int threads, size_t bytes, int dev, cudaError_t *err)
         *err = e != cudaSuccess ? e : cudaErrorInvalidConfiguration;
         return 0;
     }
-    if (cacheable) cache[dev] = blocks;
+    if (cacheable) cache[dev].store(blocks, std::memory_order_relaxed);
     return blocks;
 }
 
