@@ -832,6 +832,18 @@ __global__ void __launch_bounds__(kCfaThreads, 4) fwd_cf_async_kernel(const FwdA
         __stcs(reinterpret_cast<uint4 *>(dst), cfa_outputs<W, SILU>(E, wt, bs));
         dst += 256;
     }
+    // Interior segments whose streamed-in successor may cross the chunk's
+    // edge: checked issue, lean compute and store.
+    for (; j < jin1; ++j) {
+        cp_async_wait<kCfaSlots - 2>();
+        const uint4 v = ring_base[(j % kCfaSlots) * kCfaThreads];
+        issue_checked(j + kCfaSlots - 1);
+        cp_async_commit();
+        uint32_t E[6];
+        window(v, E);
+        __stcs(reinterpret_cast<uint4 *>(dst), cfa_outputs<W, SILU>(E, wt, bs));
+        dst += 256;
+    }
     for (; j < nseg; ++j) step_checked(j);
 
     if (chunk0 && a.st != nullptr) {
