@@ -392,6 +392,33 @@ def test_golden_rolling_after_forward():
             assert got == want, (row, got, want)
 
 
+def test_golden_spec_window_after_acceptance():
+    """The second half of the same example: after accepting k drafts, the next
+    step reads the window [h(k+1) .. hM, d1 .. dk], i.e. num_accepted_tokens
+    = k.  A unit filter (tap p = 1, no bias, no activation) makes the output
+    equal window column p, so the window is read out column by column."""
+    for row in _read_golden("spec_rolling.txt"):
+        head, after_s, tail = [p.strip() for p in row.split("|")]
+        M, N = (int(v) for v in head.split())
+        W = M + 1
+        k_s, window_s = [p.strip() for p in tail.split("->")]
+        k = int(k_s)
+        names = [f"h{i}" for i in range(1, M + 1)] + [f"d{j}" for j in range(1, N + 1)]
+        code = {n: float(i + 1) for i, n in enumerate(names)}
+        state = torch.tensor([[code[n] for n in after_s.split()]], dtype=torch.bfloat16)
+        state = state.unsqueeze(0).repeat(1, 2, 1)           # (1 line, 2 channels, M-1+N)
+        got = []
+        for p in range(W - 1):
+            weight = torch.zeros(2, W, dtype=torch.bfloat16)
+            weight[:, p] = 1.0
+            x = torch.zeros(1, 2, 1, dtype=torch.bfloat16)
+            out, err = oracle.ccv_update_spec(x, state.clone(), weight, None, None, None,
+                                              torch.tensor([k], dtype=torch.int32))
+            assert err == 0
+            got.append(float(out[0, 0, 0]))
+        assert got == [code[n] for n in window_s.split()], (row, got)
+
+
 # ---------------------------------------------------------------- decode ----
 
 @pytest.mark.parametrize("width", [2, 3, 4, 5])

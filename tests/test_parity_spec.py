@@ -133,3 +133,32 @@ def test_graph_replay_matches_eager():
     assert_bits(d["x"], eager[0], "out (in place)")
     assert_bits(d["conv_state"], eager[1], "pool")
     assert_bits(inter, eager[2], "intermediate")
+
+
+def test_golden_spec_window_after_acceptance_on_gpu():
+    """The page's rolling example (tests/golden/spec_rolling.txt) through the
+    CUDA path: unit filters read the window at num_accepted_tokens = k back
+    column by column, on 8 channels (the vector kernel)."""
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "spec_rolling.txt")
+    rows = [ln for ln in open(path) if ln.strip() and not ln.startswith("#")]
+    for row in rows:
+        head, after_s, tail = [p.strip() for p in row.split("|")]
+        M, N = (int(v) for v in head.split())
+        W = M + 1
+        k_s, window_s = [p.strip() for p in tail.split("->")]
+        names = [f"h{i}" for i in range(1, M + 1)] + [f"d{j}" for j in range(1, N + 1)]
+        code = {n: float(i + 1) for i, n in enumerate(names)}
+        cols = [code[n] for n in after_s.split()]
+        got = []
+        for p in range(W - 1):
+            state = torch.tensor(cols, dtype=torch.bfloat16, device=DEV).repeat(8, 1)
+            state = state.t().contiguous().t().unsqueeze(0)   # (1, 8, L) channels contiguous
+            weight = torch.zeros(8, W, dtype=torch.bfloat16, device=DEV)
+            weight[:, p] = 1.0
+            x = torch.zeros(1, 8, 1, dtype=torch.bfloat16, device=DEV)
+            out = ccv.ccv_update_spec(x, state, weight, None, None, None,
+                                      torch.tensor([int(k_s)], dtype=torch.int32, device=DEV))
+            torch.cuda.synchronize()
+            got.append(float(out[0, 0, 0]))
+        assert got == [code[n] for n in window_s.split()], (row, got)
