@@ -32,13 +32,6 @@ __device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
     return d;
 }
 
-// d = a * b + c per half, one rounding each.
-__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
-    f32x2 d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-
 // bf16x2 word -> (lo, hi) fp32 pair (exact).
 __device__ __forceinline__ f32x2 widen2(uint32_t w) {
     return pack2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
