@@ -261,17 +261,24 @@ __global__ void __launch_bounds__(kThreads, VEC == 8 ? 7 : 1) update_kernel(cons
             load_weights8<W>(a.w, a.ws_d, a.ws_k, c0, a.dim, a.w_vec, wpk);
             load_bias8(a.bias, c0, a.dim, a.b_vec, bs);
         }
+        // The rows' inputs do not depend on their state lines either: they go
+        // out with the index loads, so only the state windows wait for them.
+        uint4 xv[kRows];
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) {
+            const int b = rg * kRows + r;
+            xv[r] = make_uint4(0u, 0u, 0u, 0u);
+            if (active && b < a.batch) xv[r] = gather<8>(a.x + b * a.xs_b + c0 * a.xs_d, a.xs_d, a.x_vec).v;
+        }
         int lines[kRows];
         resolve_lines(a, rg, active, c0, lines);
-        uint4 win[kRows][W - 1], xv[kRows];
+        uint4 win[kRows][W - 1];
 #pragma unroll
         for (int r = 0; r < kRows; ++r) {
             if (lines[r] < 0) continue;
             const uint16_t *sp = a.st + lines[r] * a.ss_l + c0 * a.ss_d;
 #pragma unroll
             for (int j = 0; j < W - 1; ++j) win[r][j] = gather<8>(sp + j * a.ss_t, a.ss_d, a.st_vec).v;
-            const int b = rg * kRows + r;
-            xv[r] = gather<8>(a.x + b * a.xs_b + c0 * a.xs_d, a.xs_d, a.x_vec).v;
         }
         if (!active) return;
 #pragma unroll
@@ -307,11 +314,11 @@ __global__ void __launch_bounds__(kThreads, VEC == 8 ? 7 : 1) update_kernel(cons
 
 // Multi-token and speculative-verify rows, 8 channels per thread, one row
 // per thread: a chain of one memory round trip for the row's line and
-// accepted-token count (with the weights and bias), one for the window and
-// a chunk of kSpecChunk tokens of x and their output-line indices, then
-// compute and stores; longer rows repeat the chunk step.  In place (out ==
-// x) is safe: a token's x is loaded before its output is stored, by the same
-// thread, and later chunks touch other tokens.
+// accepted-token count (with the weights, bias, and the first chunk of
+// kSpecChunk tokens of x and their output-line indices), one for the
+// window, then compute and stores; longer rows load further chunks.  In
+// place (out == x) is safe: a token's x is loaded before its output is
+// stored, by the same thread, and later chunks touch other tokens.
 constexpr int kSpecThreads = 128;
 constexpr int kSpecChunk = 4;
 
@@ -328,6 +335,24 @@ __global__ void __launch_bounds__(kSpecThreads) spec_kernel(const UpdArgs a) {
     load_weights8<W>(a.w, a.ws_d, a.ws_k, c0, a.dim, a.w_vec, wpk);
     float bs[8];
     load_bias8(a.bias, c0, a.dim, a.b_vec, bs);
+    const uint16_t *xp = a.x + b * a.xs_b + c0 * a.xs_d;
+    uint4 xv[kSpecChunk];
+    int oline[kSpecChunk];
+    // A chunk of x and its output-line indices; the first goes out with the
+    // row's index loads (neither depends on the row's state line).
+    auto load_chunk = [&](int t0) {
+#pragma unroll
+        for (int u = 0; u < kSpecChunk; ++u) {
+            const int t = t0 + u;
+            xv[u] = make_uint4(0u, 0u, 0u, 0u);
+            oline[u] = -1;
+            if (t < a.seqlen) {
+                xv[u] = gather<8>(xp + t * a.xs_t, a.xs_d, a.x_vec).v;
+                if (a.oidx != nullptr) oline[u] = __ldg(a.oidx + b * a.ois_b + t * a.ois_t);
+            }
+        }
+    };
+    load_chunk(0);
     if (line == a.pad) return;
     if (line < 0 || line >= a.num_lines) {
         count_error(a.err);
@@ -339,25 +364,13 @@ __global__ void __launch_bounds__(kSpecThreads) spec_kernel(const UpdArgs a) {
         return;
     }
     uint16_t *sp = a.st + line * a.ss_l + c0 * a.ss_d;
-    const uint16_t *xp = a.x + b * a.xs_b + c0 * a.xs_d;
     uint16_t *op = a.out + b * a.os_b + c0 * a.os_d;
     uint4 win[W - 1];
 #pragma unroll
     for (int j = 0; j < W - 1; ++j) win[j] = gather<8>(sp + (off + j) * a.ss_t, a.ss_d, a.st_vec).v;
 
     for (int t0 = 0; t0 < a.seqlen; t0 += kSpecChunk) {
-        uint4 xv[kSpecChunk];
-        int oline[kSpecChunk];
-#pragma unroll
-        for (int u = 0; u < kSpecChunk; ++u) {
-            const int t = t0 + u;
-            xv[u] = make_uint4(0u, 0u, 0u, 0u);
-            oline[u] = -1;
-            if (t < a.seqlen) {
-                xv[u] = gather<8>(xp + t * a.xs_t, a.xs_d, a.x_vec).v;
-                if (a.oidx != nullptr) oline[u] = __ldg(a.oidx + b * a.ois_b + t * a.ois_t);
-            }
-        }
+        if (t0 > 0) load_chunk(t0);
         if (t0 == 0 && a.shift) {
             // Columns 0..W-3 take the window's columns 1..W-2.
 #pragma unroll
