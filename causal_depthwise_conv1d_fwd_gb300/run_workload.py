@@ -7,7 +7,8 @@ Used to give a profiler a small, self-contained program:
 Parts: prefill_tokens_dim, prefill_dim_tokens (4 x 4096 tokens, dim 8192),
 decode (256 x 8192; prefill parts take --width), paged (H16 x ws128, 32 requests; metadata + conv),
 spec (speculative verify, 64 rows x 4 drafts, dim 8192), atrex (one
-channel-first sequence of --tokens x --dim, the atrex-bench #003 shapes).
+channel-first sequence of --tokens x --dim, the atrex-bench #003 shapes),
+paged_streams (a layer's four conv streams on one paged cache, one launch).
 The process exits 0 after a device synchronize; it times nothing.
 """
 from __future__ import annotations
@@ -19,7 +20,8 @@ import torch
 from . import api
 from . import workloads as wl
 
-PARTS = ("prefill_tokens_dim", "prefill_dim_tokens", "decode", "paged", "spec", "atrex")
+PARTS = ("prefill_tokens_dim", "prefill_dim_tokens", "decode", "paged", "spec", "atrex",
+         "paged_streams")
 
 
 def _dev(kwargs, dev):
@@ -73,6 +75,16 @@ def make_launch(part: str, dev, tokens: int = 1024, dim: int = 4096, width: int 
         out = torch.empty_strided(d["x"].shape, d["x"].stride(), dtype=torch.bfloat16,
                                   device=dev)
         launch = api.prepare_ccv_fwd(**d, out=out)
+        return lambda: launch()
+    if part == "paged_streams":
+        base, streams = wl.config_paged_streams()
+        cache = base.cache.to(dev)
+        meta = {k: getattr(base, k).to(dev) for k in
+                ("positions", "block_table", "seq_idx", "slot_mapping", "query_start")}
+        ds = [{"x": st["x"].to(dev), "weight": st["weight"].to(dev), "off_s": st["off_s"],
+               "ws": st["ws"]} for st in streams]
+        launch = api.prepare_paged_sconv_fwd_streams(ds, cache, block_size=base.block_size,
+                                                     activation="silu", use_residual=True, **meta)
         return lambda: launch()
     raise ValueError(f"unknown part {part!r}; choose from {PARTS}")
 
