@@ -3,7 +3,7 @@
 Outputs within 1e-2*|ref| + 2e-5, conv_state bit-exact, untouched regions
 (pad sequences, zero-length sequences, wider state columns, guard bands)
 bit-exact.  Sizes span several chunks and ragged tails of both kernels
-(channel-last chunks of 256 tokens; channel-first chunks of 8176 tokens for
+(channel-last chunks of 256 tokens; channel-first chunks of 8056 tokens for
 aligned rows and 256 for the strided fallback).
 """
 from __future__ import annotations
@@ -120,6 +120,19 @@ def test_long_sequences_span_many_chunks(layout):
 def test_dims_not_multiple_of_eight(dim, layout):
     case = wl.varlen_prefill(400 + dim, [9, 130, 1, 45], dim, 4, num_cache_lines=5,
                              layout=layout, has_init="bernoulli")
+    check(case)
+
+
+@pytest.mark.parametrize("width", [2, 5])
+@pytest.mark.parametrize("extra", [0, 3])
+def test_channel_first_chunk_edges(width, extra):
+    """Sequences one token short of, exactly at and one past the channel-first
+    chunk length (8056 tokens) and of two chunks, on rows at several 16-byte
+    phases: the second chunk's halo and segment 0's slack (up to 127 tokens
+    before the first one needed) meet the previous chunk's last segment."""
+    case = wl.varlen_prefill(520 + width + extra, [8055, 8056, 8057, 16113, 3], 8, width,
+                             num_cache_lines=6, layout="dim_tokens", has_init="all",
+                             extra_tokens=extra)
     check(case)
 
 
