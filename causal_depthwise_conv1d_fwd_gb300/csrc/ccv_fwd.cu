@@ -132,8 +132,9 @@ __device__ __forceinline__ void stage_weights(const uint16_t *w, int64_t ws_d, i
     __syncthreads();
 }
 
-// Blocks (x < batch, y == 0) each check one sequence's indices and count
-// invalid ones; the chunk blocks skip such sequences silently.
+// The blocks of chunk slot i < batch and the first channel tile each check
+// sequence i's indices and count invalid ones; the chunk blocks skip such
+// sequences silently.  validate_sequence: slot blockIdx.x, tile blockIdx.y.
 __device__ __forceinline__ void validate_sequence_at(const FwdArgs &a, int i, bool lead) {
     if (a.err == nullptr || !lead || threadIdx.x != 0) return;
     if (i >= a.batch) return;
@@ -754,7 +755,7 @@ __global__ void __launch_bounds__(kCfaThreads, 4) fwd_cf_async_kernel(const FwdA
     const int cend = ci.start + min(ci.len, (ci.chunk + 1) * kCfaChunk);
     const bool chunk0 = ci.chunk == 0;
     const int lo = chunk0 ? cbeg : cbeg - (W - 1);
-    // x's row position on its 256-byte block (x is 2-byte aligned)
+    // where the row starts within its 256-byte block of memory, in tokens
     const int phase = static_cast<int>((reinterpret_cast<uintptr_t>(xc) >> 1) & (kCfaAlign - 1));
     // first token of segment 0: aligned, at or before the first token needed
     const int need0 = cbeg - (W - 1);
