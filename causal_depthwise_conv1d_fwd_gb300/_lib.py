@@ -16,6 +16,7 @@ P = ctypes.c_void_p
 I64 = ctypes.c_int64
 I32 = ctypes.c_int
 
+
 class PagedStream(ctypes.Structure):
     """struct ccv_paged_stream of include/ccv.h."""
     _fields_ = [("x", P), ("x_stride_t", I64), ("weight", P), ("w_stride_c", I64),

@@ -43,9 +43,18 @@ def _index_vector(t: Optional[torch.Tensor], name: str, dtype, length: Optional[
     return t
 
 
-def _stream(stream) -> ctypes.c_void_p:
+def _device_of(tensors) -> torch.device:
+    """The one device that every given tensor lives on (other items skipped)."""
+    devs = {t.device for t in tensors if isinstance(t, torch.Tensor)}
+    if len(devs) != 1:
+        raise ValueError("all tensors of a call must be on one device, got "
+                         + ", ".join(sorted(str(d) for d in devs)))
+    return devs.pop()
+
+
+def _stream(stream, device: int) -> ctypes.c_void_p:
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(device)
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
     return ctypes.c_void_p(handle)
 
@@ -66,7 +75,9 @@ def _check(status: int, where: str):
 class Launch:
     """A pre-marshalled call of one entry point: the tensors' pointers, strides
     and sizes are converted once, so each call costs one ctypes call.  The
-    tensors must stay alive and keep their storage while the plan is used."""
+    tensors must stay alive and keep their storage while the plan is used.
+    The call runs on the tensors' device (made current for the call if it is
+    not) and, by default, on that device's current stream."""
 
     def __init__(self, name: str, args: tuple, result, keep: tuple):
         self.name = name
@@ -74,9 +85,16 @@ class Launch:
         self._args = args
         self.result = result
         self._keep = keep
+        self.device = _device_of(keep).index
 
     def __call__(self, stream=None):
-        _check(self._fn(*self._args, _stream(stream)), self.name)
+        if torch.cuda.current_device() != self.device:
+            with torch.cuda.device(self.device):
+                return self._launch(stream)
+        return self._launch(stream)
+
+    def _launch(self, stream):
+        _check(self._fn(*self._args, _stream(stream, self.device)), self.name)
         return self.result
 
 

@@ -183,6 +183,17 @@ def test_binding_rejects_cpu_tensors():
         ccv.paged_sconv_fwd(**p.kwargs())
 
 
+def test_binding_requires_one_device_per_call():
+    """Every tensor of a call must live on one device; items that are not
+    tensors (the stream descriptor array) are ignored."""
+    from causal_depthwise_conv1d_fwd_gb300 import api
+
+    a, b = torch.empty(2), torch.empty(2, device="meta")
+    assert api._device_of((a, None, "descs", a)) == a.device
+    with pytest.raises(ValueError, match="one device"):
+        api._device_of((a, b))
+
+
 def test_product_path_does_not_touch_the_oracle():
     """The package must never import the oracle (no CPU fallback)."""
     import os
