@@ -1,12 +1,19 @@
-"""Host-side check of the channel-first prefill kernel's segment arithmetic.
+"""Host-side checks of the prefill kernels' work decomposition.
 
-fwd_cf_async_kernel streams a chunk's row as 256-token segments from an
-aligned start a0 and runs most of them without per-lane checks: those
-segments are loaded with unchecked 16-byte copies and stored with unchecked
-16-byte stores.  This test replays the kernel's step order (prologue issues,
-grouped lean steps, single lean steps, lean steps with a checked issue,
-checked steps) for every row phase, width and a set of sequence layouts, with
-the tiling constants read from the kernel source, and checks that:
+Chunk slots: both fast prefill kernels give block slot j to chunk k of
+sequence i when j = floor(q_i / CHUNK) + i + k, and a block finds its
+(sequence, chunk) with a warp-ballot search over query_start_loc.  A replay
+of that search checks that every chunk of every sequence gets exactly one
+slot below floor(total / CHUNK) + batch, including zero-length sequences.
+
+Channel-first segments: fwd_cf_async_kernel streams a chunk's row as
+256-token segments from an aligned start a0 and runs most of them without
+per-lane checks: those segments are loaded with unchecked 16-byte copies and
+stored with unchecked 16-byte stores.  A replay of the kernel's step order
+(prologue issues, grouped lean steps, single lean steps, lean steps with a
+checked issue, checked steps) for every row phase, width and a set of
+sequence layouts, with the tiling constants read from the kernel source,
+checks that:
 - every unchecked load and store stays inside the chunk [cbeg, cend);
 - every segment is issued once, after its ring slot was consumed, and
   consumed once, after it was issued;
@@ -28,7 +35,8 @@ def _constants():
     src = open(os.path.join(CSRC, "ccv_fwd.cu")).read()
     common = open(os.path.join(CSRC, "ccv_common.cuh")).read()
     env = {"kMaxWidth": int(re.search(r"constexpr int kMaxWidth = (\d+);", common).group(1))}
-    for name in ("kCfaSegs", "kCfaAlign", "kCfaSlots", "kCfaChunk"):
+    for name in ("kCfaSegs", "kCfaAlign", "kCfaSlots", "kCfaChunk", "kCaThreads", "kCaWarps",
+                 "kCaRun", "kCaChunk"):
         expr = re.search(rf"constexpr int {name} = ([^;]+);", src).group(1)
         env[name] = int(eval(expr, {"__builtins__": {}}, dict(env)))
     return env
@@ -139,3 +147,52 @@ def test_constants_are_the_kernels():
     """The replay uses the kernel's own constants."""
     assert K["kCfaChunk"] + K["kMaxWidth"] - 1 + K["kCfaAlign"] - 1 <= K["kCfaSegs"] * SEG
     assert K["kCfaAlign"] * 2 == 256  # tokens of 2 bytes on a 256-byte boundary
+
+
+def locate(qsl, total, C, slot):
+    """The kernels' chunk search, lane by lane: the largest sequence i with
+    floor(qsl[i] / C) + i <= slot, by rounds of a 32-lane ballot."""
+    lo, n = 0, len(qsl) - 1
+    while n > 1:
+        stride = (n + 31) >> 5
+        mask = 0
+        for lane in range(32):
+            off = lane * stride
+            if off < n and qsl[lo + off] // C + lo + off <= slot:
+                mask |= 1 << lane
+        if mask == 0:
+            break
+        top = mask.bit_length() - 1
+        lo += top * stride
+        n = min(stride, n - top * stride)
+    start, end = qsl[lo], qsl[lo + 1]
+    if start < 0 or end < start or end > total:
+        return None
+    k = slot - (start // C + lo)
+    if k < 0 or k * C >= end - start:
+        return None
+    return lo, k
+
+
+@pytest.mark.parametrize("C", ["kCaChunk", "kCfaChunk"])
+def test_chunk_slots_cover_every_chunk_once(C):
+    import random
+
+    C = K[C]
+    rng = random.Random(7)
+    for trial in range(60):
+        batch = rng.choice([1, 2, 3, 31, 32, 33, 100, 1025])
+        lens = [rng.choice([0, 1, 2, C - 1, C, C + 1, rng.randrange(0, 3 * C)])
+                for _ in range(batch)]
+        qsl = [0]
+        for n in lens:
+            qsl.append(qsl[-1] + n)
+        total = qsl[-1] + rng.choice([0, 0, 5])  # tokens past the last sequence are skipped
+        found = {}
+        for slot in range(total // C + batch):
+            r = locate(qsl, total, C, slot)
+            if r is not None:
+                assert r not in found, f"chunk {r} found by slots {found[r]} and {slot}"
+                found[r] = slot
+        want = {(i, k) for i, n in enumerate(lens) for k in range((n + C - 1) // C)}
+        assert set(found) == want
