@@ -456,6 +456,32 @@ def paged(seed: int, req_lengths: List[int], req_starts: List[int], *, H: int, w
         req_starts=list(req_starts))
 
 
+def paged_past_table(seed: int, *, H: int = 2, ws: int = 128, N: int = 16, D: int = 256,
+                     num_blocks: int = 16, off_s: int = 128, width: int = 4, top: int = 5,
+                     num_reqs: int = 3) -> PagedCase:
+    """Decode requests whose cached window lies in logical block ``top`` while
+    the block table has only ``top`` columns, so every cached tap's logical
+    block is past the table (the conv clamps it to the last column).
+
+    Request r is one token at position top*N + (width-1) + r, so its earlier
+    taps sit in block ``top``.  The table's last column points each request
+    at a physical block that no insert of the call writes, so the clamped
+    taps read data that is stable during the call.
+    """
+    if N < width - 1 + num_reqs:
+        raise ValueError("block too small for the requested positions")
+    starts = [top * N + (width - 1) + r for r in range(num_reqs)]
+    case = paged(seed, [1] * num_reqs, starts, H=H, ws=ws, N=N, D=D, num_blocks=num_blocks,
+                 off_s=off_s, width=width, name="paged_past_table")
+    written = {int(s) // N for s in case.slot_mapping.tolist() if s >= 0}
+    free = [b for b in range(num_blocks) if b not in written]
+    table = case.block_table[:, :top].clone().contiguous()
+    for r in range(num_reqs):
+        table[r, top - 1] = free[r]
+    case.block_table = table
+    return case
+
+
 def paged_mix(seed: int, num_reqs: int = 32, prefill_lo: int = 64, prefill_hi: int = 1024,
               max_start: int = 2048, N: int = 16, num_blocks: int = 1024,
               width: int = 4):

@@ -763,6 +763,27 @@ def test_paged_streams_with_equal_inputs_agree_slice_by_slice():
     assert torch.equal(cache.view(torch.int16), expected.view(torch.int16))
 
 
+def test_paged_taps_past_the_block_table_use_its_last_column():
+    """A cached tap whose logical block lies past the block table reads the
+    table's last column at the same offset in the block ("sconv.py",
+    `_fused_sconv_kernel`, the clamp to MAX_BLOCKS - 1)."""
+    case = wl.paged_past_table(151)
+    out, _, err = _run_paged(case)
+    assert err == 0
+    W, N, ws = case.weight.shape[1], case.block_size, case.ws
+    last = case.block_table.shape[1] - 1
+    for r in range(case.T):
+        p0 = int(case.positions[r])
+        cols = []
+        for src in range(p0 - (W - 1), p0):
+            assert src // N > last
+            blk = int(case.block_table[r, last])
+            cols.append(case.cache[blk, :, src % N, case.off_s:case.off_s + ws].reshape(-1))
+        xs = case.x[r:r + 1].t()
+        ref = r1_reference(xs, case.weight, None, torch.stack(cols, dim=1), True)
+        assert_bf16_close(out[r:r + 1].t(), ref + xs.to(torch.float64))
+
+
 def test_paged_invalid_block_is_counted():
     case = _small_paged(171, [2, 1], [5, 9])
     case.block_table[1, :] = 10_000

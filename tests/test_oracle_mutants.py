@@ -45,6 +45,7 @@ MUTANTS = [
     ("paged_insert_no_stream_offset", "(slot % N) * cs_n + off_s + c % ws] =",
      "(slot % N) * cs_n + c % ws] ="),
     ("paged_pad_not_masked", "int real = slot_mapping[t] >= 0;", "int real = 1;"),
+    ("paged_block_not_clamped", "if (lblk > max_blocks - 1) lblk = max_blocks - 1;", ""),
     ("metadata_strict", "if (query_start_loc[j] <= t) owner = j;",
      "if (query_start_loc[j] < t) owner = j;"),
     ("spec_offset_is_count", "num_accepted_tokens[b] - 1 : 0", "num_accepted_tokens[b] : 0"),

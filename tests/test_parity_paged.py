@@ -47,6 +47,11 @@ def test_config_paged_full_size():
     check(wl.config_paged())
 
 
+def test_taps_past_the_block_table_are_clamped():
+    """Cached taps whose logical block lies past the table read its last column."""
+    check(wl.paged_past_table(161))
+
+
 def test_config_paged_metadata_full_size():
     case = wl.config_paged()
     seq = torch.full((case.T + 8,), 77, dtype=torch.int32, device=DEV)
