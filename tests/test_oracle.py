@@ -679,6 +679,29 @@ def test_paged_pad_rows_are_residual_or_zero():
         assert bool((out2[t].float() == 0).all())
 
 
+def test_paged_in_forward_taps_read_pad_rows_of_their_request():
+    """An in-forward tap reads x even when that row is a PAD row (the tap rule
+    of "sconv.py" decides by row >= query_start only); PAD rows themselves
+    give the residual."""
+    case = _small_paged(145, [9, 6, 3], [2, 11, 0], interior_pad_frac=0.3)
+    pads = set((case.slot_mapping < 0).nonzero().flatten().tolist())
+    assert pads, "the case must hold interior PAD rows"
+    out, _, err = _run_paged(case)
+    assert err == 0
+    q = case.query_start_loc.tolist()
+    hit = 0
+    for r in range(len(case.req_lengths)):
+        xs = case.x[q[r]:q[r + 1]].t()
+        ref = r1_reference(xs, case.weight, None, _history(case, r, 4), True)
+        ref = ref + xs.to(torch.float64)
+        for i, t in enumerate(range(q[r], q[r + 1])):
+            if t in pads:
+                continue
+            hit += any(row in pads for row in range(max(q[r], t - 3), t))
+            assert_bf16_close(out[t:t + 1].t(), ref[:, i:i + 1])
+    assert hit, "some real token must have a PAD row in its window"
+
+
 def test_paged_split_requests_equal_one_forward():
     """Running each request's tokens as several consecutive forwards (cache
     carried between them) gives the same outputs and cache as one forward."""

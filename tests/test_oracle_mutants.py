@@ -46,6 +46,8 @@ MUTANTS = [
      "(slot % N) * cs_n + c % ws] ="),
     ("paged_pad_not_masked", "int real = slot_mapping[t] >= 0;", "int real = 1;"),
     ("paged_block_not_clamped", "if (lblk > max_blocks - 1) lblk = max_blocks - 1;", ""),
+    ("paged_pad_row_tap_zeroed", "v = bf16_to_f32(x[row * xs_t + c]);",
+     "v = slot_mapping[row] >= 0 ? bf16_to_f32(x[row * xs_t + c]) : 0.0f;"),
     ("metadata_strict", "if (query_start_loc[j] <= t) owner = j;",
      "if (query_start_loc[j] < t) owner = j;"),
     ("spec_offset_is_count", "num_accepted_tokens[b] - 1 : 0", "num_accepted_tokens[b] : 0"),
