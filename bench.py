@@ -114,24 +114,32 @@ def paged_bytes(case) -> int:
 
 
 def _paged_bytes(case) -> int:
+    """x read + out write for every row, the insert of every real token, each
+    distinct cached (request, position) the pre-forward taps read, each
+    distinct block-table entry those reads resolve through, the weights, the
+    four per-token index values and the query_start_loc of the metadata."""
     C = case.x.shape[1]
     W = case.weight.shape[1]
     T = case.T
+    N = case.block_size
+    max_blocks = case.block_table.shape[1]
     real = (case.slot_mapping >= 0)
     n_real = int(real.sum())
-    cached_taps = 0
+    cached, entries = set(), set()
     for t in range(T):
         if not bool(real[t]):
             continue
         pos = int(case.positions[t])
         qs = int(case.query_start[t])
+        req = int(case.seq_idx[t])
         for iw in range(W):
             src = pos - (W - 1) + iw
             row = t - (W - 1) + iw
             if src >= 0 and row < qs:
-                cached_taps += 1
-    return (2 * T * C * 2 + n_real * C * 2 + cached_taps * C * 2 + C * W * 2
-            + T * (8 + 4 + 8 + 4) + cached_taps * 4 + 4 * (len(case.req_lengths) + 1))
+                cached.add((req, src))
+                entries.add((req, min(src // N, max_blocks - 1)))
+    return (2 * T * C * 2 + n_real * C * 2 + len(cached) * C * 2 + C * W * 2
+            + T * (8 + 4 + 8 + 4) + len(entries) * 4 + 4 * (len(case.req_lengths) + 1))
 
 
 # ---------------------------------------------------------------- clocks ----

@@ -43,6 +43,18 @@ def _index_vector(t: Optional[torch.Tensor], name: str, dtype, length: Optional[
     return t
 
 
+def _bias_vector(bias: Optional[torch.Tensor], dim: int):
+    """The C ABI reads bias as `dim` contiguous values: reject any other
+    shape or a strided view (a column of a packed parameter, say)."""
+    if bias is None:
+        return None
+    if bias.shape != (dim,):
+        raise ValueError(f"bias must have shape ({dim},), got {tuple(bias.shape)}")
+    if dim > 1 and bias.stride(0) != 1:
+        raise ValueError(f"bias must be contiguous (stride 1), got stride {bias.stride(0)}")
+    return bias
+
+
 def _device_of(tensors) -> torch.device:
     """The one device that every given tensor lives on (other items skipped)."""
     devs = {t.device for t in tensors if isinstance(t, torch.Tensor)}
@@ -126,8 +138,9 @@ def prepare_ccv_fwd(x, weight, bias, conv_states, query_start_loc, cache_indices
         raise ValueError("x must be (dim, total_tokens) and weight (dim, width)")
     dim, total = x.shape
     width = weight.shape[1]
-    if weight.shape[0] != dim or (bias is not None and bias.shape != (dim,)):
-        raise ValueError("weight / bias do not match dim")
+    if weight.shape[0] != dim:
+        raise ValueError("weight does not match dim")
+    bias = _bias_vector(bias, dim)
     qsl = _index_vector(query_start_loc, "query_start_loc", torch.int32)
     batch = qsl.numel() - 1
     ci = _index_vector(cache_indices, "cache_indices", torch.int32, batch)
@@ -187,6 +200,7 @@ def prepare_ccv_update(x, conv_state, weight, bias=None, activation=None,
     width = weight.shape[1]
     if weight.shape[0] != dim or conv_state.dim() != 3 or conv_state.shape[1] != dim:
         raise ValueError("weight / conv_state do not match dim")
+    bias = _bias_vector(bias, dim)
     if out is None:
         out3 = x3
     else:
@@ -245,6 +259,7 @@ def prepare_ccv_update_spec(x, conv_state, weight, bias=None, activation=None,
     width = weight.shape[1]
     if weight.shape[0] != dim or conv_state.dim() != 3 or conv_state.shape[1] != dim:
         raise ValueError("weight / conv_state do not match dim")
+    bias = _bias_vector(bias, dim)
     if out is None:
         out3 = x3
     else:

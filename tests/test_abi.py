@@ -252,3 +252,20 @@ def test_missing_library_fails_loudly(tmp_path):
                           cwd=os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
     assert proc.returncode == 0, proc.stderr
     assert "not built" in proc.stdout
+
+
+def test_binding_rejects_a_strided_or_misshapen_bias():
+    """The C ABI reads bias as dim contiguous values, so the binding refuses a
+    strided view (a column of a packed parameter) and a wrong length instead
+    of passing a pointer the kernels would misread."""
+    from causal_depthwise_conv1d_fwd_gb300 import api
+
+    packed = torch.zeros(16, 3)
+    assert api._bias_vector(None, 16) is None
+    assert api._bias_vector(packed[:, 0].contiguous(), 16) is not None
+    with pytest.raises(ValueError, match="contiguous"):
+        api._bias_vector(packed[:, 1], 16)
+    with pytest.raises(ValueError, match="shape"):
+        api._bias_vector(torch.zeros(15), 16)
+    # a single channel has no stride to get wrong
+    assert api._bias_vector(packed[:1, 2], 1) is not None

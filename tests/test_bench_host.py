@@ -32,11 +32,22 @@ def test_decode_bytes_match_the_stated_figure():
 
 
 def test_paged_bytes_count_cached_taps():
-    # one decode token at position 10 (3 cached taps) and one prefill of 2
-    # tokens starting at 0 (no taps before position 0)
+    # one decode token at position 10 (3 cached taps: positions 7, 8, 9 in
+    # blocks 1, 2, 2 of size 4) and one prefill of 2 tokens starting at 0 (no
+    # taps before position 0)
     case = wl.paged(3, [1, 2], [10, 0], H=1, ws=8, N=4, D=8, num_blocks=8, off_s=0)
     C, T = 8, 3
-    want = 2 * T * C * 2 + 3 * C * 2 + 3 * C * 2 + C * 4 * 2 + T * 24 + 3 * 4 + 4 * 3
+    want = 2 * T * C * 2 + 3 * C * 2 + 3 * C * 2 + C * 4 * 2 + T * 24 + 2 * 4 + 4 * 3
+    assert bench.paged_bytes(case) == want
+
+
+def test_paged_bytes_count_each_cached_position_once():
+    # a 4-token spec request at position 10: its first three tokens read
+    # 3 + 2 + 1 cached taps, but only positions 7, 8 and 9 (block-table
+    # entries 1 and 2) need to be read
+    case = wl.paged(4, [4], [10], H=1, ws=8, N=4, D=8, num_blocks=8, off_s=0)
+    C, T = 8, 4
+    want = 2 * T * C * 2 + 4 * C * 2 + 3 * C * 2 + C * 4 * 2 + T * 24 + 2 * 4 + 4 * 2
     assert bench.paged_bytes(case) == want
 
 

@@ -331,3 +331,20 @@ def test_cuda_graph_replay_matches_eager():
                    c2.has_initial_state, c2.activation, -1, out=ref_out)
     assert_close(out, ref_out, "graph out")
     assert_bits(d["conv_states"], ref_states, "graph states")
+
+
+def test_strided_bias_is_rejected():
+    """bias is read as dim contiguous values: a strided view raises in the
+    binding for prefill, decode and spec-verify alike (no silent misread)."""
+    case = wl.varlen_prefill(1601, [5, 9], 64, 4, num_cache_lines=2)
+    d = to_device(case.kwargs(), DEV)
+    packed = torch.zeros(64, 2, dtype=torch.bfloat16, device=DEV)
+    d["bias"] = packed[:, 1]
+    with pytest.raises(ValueError, match="contiguous"):
+        ccv.ccv_fwd(**d)
+    dc = to_device(wl.decode(1602, 4, 64, 4, num_lines=4).kwargs(), DEV)
+    dc["bias"] = packed[:, 0]
+    with pytest.raises(ValueError, match="contiguous"):
+        ccv.ccv_update(**dc)
+    with pytest.raises(ValueError, match="contiguous"):
+        ccv.ccv_update_spec(**dc)
