@@ -342,10 +342,17 @@ def measured_peak_hbm():
 # --------------------------------------------------------------- our arm ----
 
 class Part:
-    def __init__(self, name, kernel, launches, nbytes, tokens, fn):
+    """One part of the step: `fn_on(handle)` enqueues its launches on the
+    given stream handle, `fn()` on the stream current at set-up."""
+
+    def __init__(self, name, kernel, launches, nbytes, tokens, fn_on, stream):
         self.name, self.kernel, self.launches = name, kernel, launches
-        self.nbytes, self.tokens, self.fn = nbytes, tokens, fn
+        self.nbytes, self.tokens, self.fn_on = nbytes, tokens, fn_on
+        self.stream = stream
         self.ms = 0.0
+
+    def fn(self):
+        self.fn_on(self.stream)
 
 
 def make_parts(dev, rank):
@@ -370,14 +377,12 @@ def make_parts(dev, rank):
         dev_args[name] = (d, out)
         launch = ccv.prepare_ccv_fwd(**d, out=out)
         parts.append(Part(name, "fwd_cl_async_kernel" if name.endswith("tokens_dim") else "fwd_cf_async_kernel",
-                          1, prefill_bytes(c), prefill_tokens(c),
-                          (lambda launch=launch: launch(stream))))
+                          1, prefill_bytes(c), prefill_tokens(c), launch, stream))
     c = cases["decode"]
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in c.kwargs().items()}
     dev_args["decode"] = (d, d["x"])
     launch = ccv.prepare_ccv_update(**d)
-    parts.append(Part("decode", "update_kernel", 1, decode_bytes(c), c.x.shape[0],
-                      (lambda launch=launch: launch(stream))))
+    parts.append(Part("decode", "update_kernel", 1, decode_bytes(c), c.x.shape[0], launch, stream))
     c = cases["paged"]
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in c.kwargs().items()}
     qsl = c.query_start_loc.to(dev)
@@ -390,11 +395,11 @@ def make_parts(dev, rank):
     meta = ccv.prepare_paged_sconv_seq_metadata(qsl, n_req, c.num_actual_tokens, seq, qs, c.T)
     conv = ccv.prepare_paged_sconv_fwd(**d, out=out)
 
-    def paged_step(meta=meta, conv=conv):
-        meta(stream)
-        conv(stream)
+    def paged_step(handle, meta=meta, conv=conv):
+        meta(handle)
+        conv(handle)
 
-    parts.append(Part("paged", "paged_vec_kernel", 2, paged_bytes(c), c.T, paged_step))
+    parts.append(Part("paged", "paged_vec_kernel", 2, paged_bytes(c), c.T, paged_step, stream))
     return parts, cases, dev_args
 
 
@@ -767,6 +772,117 @@ def small_configs_timing(dev, calls=100):
     return rows
 
 
+def time_parts(parts, steps, stream):
+    """K steps with an event between parts: adds each part's time to p.ms and
+    returns the seconds of the whole loop."""
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(len(parts) + 1)]
+              for _ in range(steps)]
+    torch.cuda.synchronize()
+    for s in range(steps):
+        ev = events[s]
+        ev[0].record(stream)
+        for i, p in enumerate(parts):
+            p.fn()
+            ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    for s in range(steps):
+        for i, p in enumerate(parts):
+            p.ms += events[s][i].elapsed_time(events[s][i + 1])
+    return events[0][0].elapsed_time(events[-1][-1]) / 1e3
+
+
+def graph_step_timing(parts, steps):
+    """The step captured as one CUDA graph and replayed K times: ms per step,
+    and each part's us per call from timing events recorded inside the graph
+    (where this torch records events as graph nodes; their nodes also
+    serialise the launches around them, so the part figures add up to more
+    than the event-free step)."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+
+    def capture(with_events):
+        g = torch.cuda.CUDAGraph()
+        evs = None
+        with torch.cuda.graph(g, stream=s):
+            if with_events:
+                evs = [torch.cuda.Event(enable_timing=True, external=True)
+                       for _ in range(len(parts) + 1)]
+                evs[0].record()
+            for i, p in enumerate(parts):
+                p.fn_on(torch.cuda.current_stream().cuda_stream)
+                if with_events:
+                    evs[i + 1].record()
+        return g, evs
+
+    def replay(g, n):
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(n):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n
+
+    g, _ = capture(False)
+    out = {"ms_per_step": round(replay(g, steps), 4)}
+    del g
+    try:
+        g, evs = capture(True)
+    except TypeError:  # this torch cannot record timing events as graph nodes
+        return out
+    n = min(steps, 200)
+    per = [0.0] * len(parts)
+    for _ in range(n):
+        g.replay()
+        torch.cuda.synchronize()
+        for i in range(len(parts)):
+            per[i] += evs[i].elapsed_time(evs[i + 1])
+    out["parts_us"] = {p.name: round(per[i] * 1e3 / n, 2) for i, p in enumerate(parts)}
+    return out
+
+
+def host_link_peak(dev, nbytes=1 << 30, reps=5):
+    """Plain copies between pinned host memory and the device, best of
+    `reps`: one `nbytes` buffer host->device, device->host, and both at once
+    on two streams.  GB/s of bytes moved (both directions for the last)."""
+    h_in = torch.ones(nbytes, dtype=torch.uint8).pin_memory()
+    h_out = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d_in = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    d_out = torch.ones(nbytes, dtype=torch.uint8, device=dev)
+    cur = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def timed(h2d, d2h):
+        best = float("inf")
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(cur)
+            s_in.wait_stream(cur)
+            s_out.wait_stream(cur)
+            if h2d:
+                with torch.cuda.stream(s_in):
+                    d_in.copy_(h_in, non_blocking=True)
+            if d2h:
+                with torch.cuda.stream(s_out):
+                    h_out.copy_(d_out, non_blocking=True)
+            cur.wait_stream(s_in)
+            cur.wait_stream(s_out)
+            b.record(cur)
+            torch.cuda.synchronize()
+            best = min(best, a.elapsed_time(b) / 1e3)
+        return (int(h2d) + int(d2h)) * nbytes / best / 1e9
+
+    out = {"h2d_gbs": round(timed(True, False), 1), "d2h_gbs": round(timed(False, True), 1),
+           "both_gbs": round(timed(True, True), 1), "buffer_bytes": nbytes}
+    del h_in, h_out, d_in, d_out
+    return out
+
+
 def run_ours(args):
     import causal_depthwise_conv1d_fwd_gb300 as ccv  # noqa: F401
     from causal_depthwise_conv1d_fwd_gb300 import _lib
@@ -787,9 +903,9 @@ def run_ours(args):
             p.fn()
     torch.cuda.synchronize()
 
-    n_ev = len(parts) + 1
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
-              for _ in range(args.steps)]
+    # The headline: K steps back to back with nothing between the launches,
+    # so each kernel's launch may overlap the previous one's tail (every
+    # kernel of the library is launched with programmatic serialization).
     sampler = ClockSampler(dev)
     if rank == 0:
         sampler.start()
@@ -799,22 +915,21 @@ def run_ours(args):
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
-    for s in range(args.steps):
-        ev = events[s]
-        ev[0].record(stream)
-        for i, p in enumerate(parts):
+    for _ in range(args.steps):
+        for p in parts:
             p.fn()
-            ev[i + 1].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
     sampler.mark("end")
     barrier(dev)
     seconds = t_start.elapsed_time(t_end) / 1e3
-    for s in range(args.steps):
-        for i, p in enumerate(parts):
-            p.ms += events[s][i].elapsed_time(events[s][i + 1])
     clocks = sampler.stop() if rank == 0 else None
     max_seconds = max_over_ranks(seconds, dev)
+
+    # The parts: the same K steps again with an event between parts (an
+    # event between two launches also serialises them).
+    parts_s = time_parts(parts, args.steps, stream)
+    graph = graph_step_timing(parts, args.steps)
 
     step_bytes = sum(p.nbytes for p in parts)
     value = whole_job_rate(step_bytes, args.steps, world, max_seconds) / 1e9
@@ -832,6 +947,8 @@ def run_ours(args):
     e2e_s, h2d, d2h = run_e2e(dev, cases, dev_args, e2e_steps)
     e2e_s = max_over_ranks(e2e_s, dev)
     e2e_value = whole_job_rate(step_bytes, e2e_steps, world, e2e_s) / 1e9
+    link = host_link_peak(dev)
+    link_gbs = (h2d + d2h) * e2e_steps / e2e_s / 1e9
     graph_us = decode_graph_us(dev_args)
     spec = spec_verify_timing(dev, rank)
     atrex = atrex_shapes_timing(dev)
@@ -854,6 +971,8 @@ def run_ours(args):
         if p.name == "decode":
             entry["us_per_call_l2_cold"] = round(us, 2)
             entry["us_per_call_graph_warm"] = round(graph_us, 2)
+        if "parts_us" in graph:
+            entry["us_in_graph_step"] = graph["parts_us"][p.name]
         parts_out[p.name] = entry
     line = {
         "metric": METRIC,
@@ -863,6 +982,8 @@ def run_ours(args):
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(max_seconds * 1e3 / args.steps, 4),
+        "graph_step": graph,
+        "parts_loop_ms_per_step": round(parts_s * 1e3 / args.steps, 4),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -889,7 +1010,9 @@ def run_ours(args):
                      "algorithmic_bytes_per_launch": dominant.nbytes // dominant.launches,
                      "avg_launch_us": round(dom_us, 2)},
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "steps": e2e_steps,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "link_gbs": round(link_gbs, 1), "link_peak_gbs": link["both_gbs"],
+                "frac_of_link": round(link_gbs / link["both_gbs"], 4), "link_peak": link},
         "gpu_launches": sum(p.launches for p in parts) * args.steps,
         "clocks": clocks,
         "cpu_baseline": cpu,

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <atomic>
+#include <utility>
 
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -96,6 +97,23 @@ __device__ __forceinline__ void store_plain(uint16_t *p, const Raw<VEC> &r) {
     else *p = r.v;
 }
 
+// ------------------------------------------ programmatic dependent launch ----
+//
+// Every kernel of the library is launched with programmatic stream
+// serialization (launch_pdl below): it may be scheduled while the previous
+// kernel of the stream is still finishing, so its launch and block set-up
+// overlap that kernel's tail.  Such a kernel must not touch global memory --
+// no read and no write, since the previous kernel may still read what this
+// one overwrites -- before wait_prior_grid(), which returns once the previous
+// kernel has completed and its writes are visible.  release_next_grid() lets
+// the next kernel of the stream be scheduled; it only ever starts early, and
+// it waits in its own wait_prior_grid() for this kernel to complete.  Without
+// a programmatic predecessor the wait returns at once.
+__device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void release_next_grid() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------- numerics ----
 
 __device__ __forceinline__ float rcp_approx(float x) {
@@ -185,6 +203,29 @@ inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 inline int launch_status() {
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? CCV_OK : static_cast<int>(e);
+}
+
+// Launch `kernel` on `stream` with programmatic stream serialization (see
+// wait_prior_grid).  Returns CCV_OK or the cudaError_t of the launch.
+template <typename... Params, typename... Args>
+inline int launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                      cudaStream_t stream, Args &&...args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+    if (e != cudaSuccess) {
+        cudaGetLastError();  // the error is returned; do not leave it for the next call
+        return static_cast<int>(e);
+    }
+    return launch_status();
 }
 
 // Byte range [lo, hi] covered by a strided 2-D or 3-D bf16 view (strides >= 0).

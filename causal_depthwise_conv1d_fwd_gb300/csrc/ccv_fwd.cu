@@ -215,6 +215,8 @@ __global__ void __launch_bounds__(kThreads) fwd_cl_kernel(const FwdArgs a) {
     constexpr int TILE_C = 32 * VEC;
     __shared__ __align__(16) uint16_t s_w[W * TILE_C];
     __shared__ __align__(16) uint16_t s_b[TILE_C];
+    release_next_grid();
+    wait_prior_grid();
     validate_sequence(a);
     ChunkInfo ci;
     if (!locate_chunk(a, kClChunk, blockIdx.x, ci)) return;
@@ -307,6 +309,8 @@ template <int W, bool SILU, int VEC>
 __global__ void __launch_bounds__(kThreads) fwd_cf_kernel(const FwdArgs a) {
     constexpr int SEG = 32 * VEC;
     constexpr int CHUNK = kCfSegs * SEG;
+    release_next_grid();
+    wait_prior_grid();
     validate_sequence(a);
     ChunkInfo ci;
     if (!locate_chunk(a, CHUNK, blockIdx.x, ci)) return;
@@ -514,6 +518,8 @@ __global__ void __launch_bounds__(kCaThreads, W == 5 ? 2 : 3) fwd_cl_async_kerne
     extern __shared__ __align__(16) uint4 s_ring[];  // [kCaSlots][kCaThreads]
     __shared__ __align__(16) uint16_t s_w[W * kCaTileC];
     __shared__ __align__(16) uint16_t s_b[kCaTileC];
+    release_next_grid();
+    wait_prior_grid();
     // One-dimensional grid, block = slot * tiles + tile: channel tiles vary
     // fastest in launch order, so the blocks resident at one time read whole
     // token rows (3% faster than chunk-major order, measured).
@@ -742,6 +748,8 @@ __device__ __forceinline__ uint4 cfa_outputs(const uint32_t (&E)[6], const uint3
 template <int W, bool SILU>
 __global__ void __launch_bounds__(kCfaThreads, 4) fwd_cf_async_kernel(const FwdArgs a) {
     extern __shared__ __align__(16) uint4 s_ring[];  // [kCfaSlots][kCfaThreads]
+    release_next_grid();
+    wait_prior_grid();
     validate_sequence(a);
     ChunkInfo ci;
     if (!locate_chunk(a, kCfaChunk, blockIdx.x, ci)) return;
@@ -955,8 +963,8 @@ int launch_cl_async_w(const FwdArgs &a, cudaStream_t stream) {
     const int64_t blocks = (static_cast<int64_t>(a.total) / kCaChunk + a.batch) *
                            ((a.dim + kCaTileC - 1) / kCaTileC);
     if (blocks > 0x7fffffff) return CCV_ERR_SIZE;
-    fwd_cl_async_kernel<W, SILU><<<static_cast<unsigned>(blocks), kCaThreads, kCaSmem, stream>>>(a);
-    return launch_status();
+    return launch_pdl(fwd_cl_async_kernel<W, SILU>, dim3(static_cast<unsigned>(blocks)),
+                      dim3(kCaThreads), kCaSmem, stream, a);
 }
 
 template <int W, bool SILU>
@@ -969,8 +977,7 @@ int launch_cf_async_w(const FwdArgs &a, cudaStream_t stream) {
     const dim3 grid(static_cast<unsigned>(a.total / kCfaChunk + a.batch),
                     static_cast<unsigned>((a.dim + kCfaWarps - 1) / kCfaWarps));
     if (grid.y > 65535u) return CCV_ERR_SIZE;
-    fwd_cf_async_kernel<W, SILU><<<grid, kCfaThreads, kCfaSmem, stream>>>(a);
-    return launch_status();
+    return launch_pdl(fwd_cf_async_kernel<W, SILU>, grid, dim3(kCfaThreads), kCfaSmem, stream, a);
 }
 
 int launch_cl_async(const FwdArgs &a, int width, bool silu, cudaStream_t stream) {
@@ -1077,6 +1084,5 @@ extern "C" int ccv_fwd(const void *x, int64_t x_stride_dim, int64_t x_stride_tok
                     static_cast<unsigned>((dim + 31) / 32));
     }
     if (grid.y > 65535u) return CCV_ERR_SIZE;
-    fn<<<grid, kThreads, 0, stream>>>(a);
-    return launch_status();
+    return launch_pdl(fn, grid, dim3(kThreads), 0, stream, a);
 }

@@ -248,6 +248,8 @@ __device__ __forceinline__ void general_rows(const UpdArgs &a, int rg, int c0, c
 // path: any seqlen, the spec extras, fp32 arithmetic.
 template <int W, bool SILU, int VEC>
 __global__ void __launch_bounds__(kThreads, VEC == 8 ? 7 : 1) update_kernel(const UpdArgs a) {
+    release_next_grid();
+    wait_prior_grid();
     constexpr int TILE_C = kThreads * VEC;
     const int rg = blockIdx.x / a.ctiles;
     const int ct = blockIdx.x - rg * a.ctiles;
@@ -324,6 +326,8 @@ constexpr int kSpecChunk = 4;
 
 template <int W, bool SILU>
 __global__ void __launch_bounds__(kSpecThreads) spec_kernel(const UpdArgs a) {
+    release_next_grid();
+    wait_prior_grid();
     const int b = blockIdx.x / a.ctiles;
     const int ct = blockIdx.x - b * a.ctiles;
     const int c0 = ct * kSpecThreads * 8 + threadIdx.x * 8;
@@ -552,16 +556,14 @@ int update_launch(const void *x, int64_t x_stride_b, int64_t x_stride_dim, int64
         a.ctiles = (dim + kSpecThreads * 8 - 1) / (kSpecThreads * 8);
         const int64_t blocks = static_cast<int64_t>(batch) * a.ctiles;
         if (blocks > 0x7fffffffLL) return CCV_ERR_SIZE;
-        pick_spec_kernel(width, silu != 0)<<<static_cast<unsigned>(blocks), kSpecThreads, 0,
-                                             stream>>>(a);
-        return launch_status();
+        return launch_pdl(pick_spec_kernel(width, silu != 0), dim3(static_cast<unsigned>(blocks)),
+                          dim3(kSpecThreads), 0, stream, a);
     }
     a.ctiles = (dim + kThreads * vw - 1) / (kThreads * vw);
     const int64_t blocks = static_cast<int64_t>((batch + kRows - 1) / kRows) * a.ctiles;
     if (blocks > 0x7fffffffLL) return CCV_ERR_SIZE;
     KernelFn fn = vec ? pick_kernel<8>(width, silu != 0) : pick_kernel<1>(width, silu != 0);
-    fn<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(a);
-    return launch_status();
+    return launch_pdl(fn, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, stream, a);
 }
 
 }  // namespace

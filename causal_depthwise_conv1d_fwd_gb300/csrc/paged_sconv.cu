@@ -188,6 +188,8 @@ __device__ __forceinline__ int64_t shfl64(int64_t v, int src) {
 // Fallback for unaligned or odd-width layouts: one channel per lane.
 template <int W, bool SILU, bool RESID>
 __global__ void __launch_bounds__(kThreads) paged_scalar_kernel(const PagedArgs a) {
+    release_next_grid();
+    wait_prior_grid();
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int t0 = blockIdx.x * kBlockTokens + warp * kRun;
@@ -312,6 +314,8 @@ __device__ __forceinline__ uint4 paged_row(const uint4 (&wpk)[W], const uint4 (&
 template <int W, bool SILU, bool RESID>
 __global__ void __launch_bounds__(kThreads, 7) paged_vec_kernel(const PagedLaunch pl) {
     extern __shared__ uint4 stage[];
+    release_next_grid();
+    wait_prior_grid();
     constexpr int R = kVecRun + W - 1;
     PagedArgs a = pl.a;
     if (gridDim.z > 1) {
@@ -500,6 +504,8 @@ constexpr int kMetaThreads = 256;
 __global__ void __launch_bounds__(kMetaThreads)
 seq_metadata_kernel(const int32_t *qsl, int num_reqs, int num_actual, int num_padded,
                     int32_t *seq_idx, int32_t *query_start) {
+    release_next_grid();
+    wait_prior_grid();
     const int t = blockIdx.x * kMetaThreads + threadIdx.x;
     if (t >= num_padded) return;
     if (t >= num_actual) {
@@ -535,10 +541,9 @@ extern "C" int paged_sconv_seq_metadata(const int32_t *query_start_loc, int num_
         (num_actual_tokens > 0 && query_start_loc == nullptr))
         return CCV_ERR_NULL_POINTER;
     const int blocks = (num_padded_tokens + kMetaThreads - 1) / kMetaThreads;
-    seq_metadata_kernel<<<blocks, kMetaThreads, 0, stream>>>(
-        query_start_loc, num_reqs, num_actual_tokens, num_padded_tokens, seq_idx_out,
-        query_start_out);
-    return launch_status();
+    return launch_pdl(seq_metadata_kernel, dim3(blocks), dim3(kMetaThreads), 0, stream,
+                      query_start_loc, num_reqs, num_actual_tokens, num_padded_tokens, seq_idx_out,
+                      query_start_out);
 }
 
 namespace ccv {
@@ -641,8 +646,8 @@ int launch_vec(const PagedShared &p, const ccv_paged_stream *streams, int n, ccv
                     static_cast<unsigned>((max_c + kVecChannels - 1) / kVecChannels),
                     static_cast<unsigned>(n));
     if (grid.y > 65535u) return CCV_ERR_SIZE;
-    pick_vec(p.width, p.silu != 0, p.residual != 0)<<<grid, kThreads, vec_smem(p.width), stream>>>(pl);
-    return launch_status();
+    return launch_pdl(pick_vec(p.width, p.silu != 0, p.residual != 0), grid, dim3(kThreads),
+                      vec_smem(p.width), stream, pl);
 }
 
 int launch_scalar(const PagedShared &p, const ccv_paged_stream &st, ccv_stream_t stream) {
@@ -651,8 +656,8 @@ int launch_scalar(const PagedShared &p, const ccv_paged_stream &st, ccv_stream_t
     const dim3 grid(static_cast<unsigned>((p.T + kBlockTokens - 1) / kBlockTokens),
                     static_cast<unsigned>((a.C + 31) / 32));
     if (grid.y > 65535u) return CCV_ERR_SIZE;
-    pick_scalar(p.width, p.silu != 0, p.residual != 0)<<<grid, kThreads, 0, stream>>>(a);
-    return launch_status();
+    return launch_pdl(pick_scalar(p.width, p.silu != 0, p.residual != 0), grid, dim3(kThreads), 0,
+                      stream, a);
 }
 
 int paged_run(const PagedShared &p, const ccv_paged_stream *streams, int n, ccv_stream_t stream) {
