@@ -287,7 +287,7 @@ KERNEL_SOURCE = {
     "fwd_cf_async_kernel": "ccv_fwd.cu",
     "update_kernel": "ccv_update.cu",
     "spec_kernel": "ccv_update.cu",
-    "paged_vec_kernel": "paged_sconv.cu",
+    "paged_row_kernel": "paged_sconv.cu",
     "seq_metadata_kernel": "paged_sconv.cu",
 }
 
@@ -399,7 +399,7 @@ def make_parts(dev, rank):
         meta(handle)
         conv(handle)
 
-    parts.append(Part("paged", "paged_vec_kernel", 2, paged_bytes(c), c.T, paged_step, stream))
+    parts.append(Part("paged", "paged_row_kernel", 2, paged_bytes(c), c.T, paged_step, stream))
     return parts, cases, dev_args
 
 
@@ -689,7 +689,7 @@ def paged_streams_timing(dev, calls=100):
     us_sep = timed(lambda: [launch(stream) for launch in single])
     # every stream has the base case's channel count and token metadata
     nbytes = len(streams) * _paged_bytes(base)
-    return {"workload": base.name, "kernel": "paged_vec_kernel", "streams": len(streams),
+    return {"workload": base.name, "kernel": "paged_row_kernel", "streams": len(streams),
             "bytes": nbytes, "us_fused_l2_cold": round(us_fused, 2),
             "us_separate_l2_cold": round(us_sep, 2),
             "gbs_fused": round(nbytes / (us_fused * 1e-6) / 1e9, 1)}

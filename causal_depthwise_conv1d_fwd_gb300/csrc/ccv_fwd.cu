@@ -29,6 +29,20 @@
 // A VEC = 1 instantiation of each handles unaligned or arbitrary strides.
 // Accumulation is fp32 in the pages' order (bias first, taps 0..W-1), SiLU
 // in fp32, one round-to-nearest-even store to bf16.
+//
+// Short problems (total_tokens * dim up to kShortMaxElems) take two more
+// kernels, one per layout, built for latency instead of streaming.
+//
+// The note on the streaming kernels' launches.  Every kernel is launched
+// with programmatic stream serialization and waits for its predecessor
+// before touching memory.  The streaming kernels do not release their own
+// successor early: they run many waves, and letting the next kernel take
+// their SMs during their last wave made a bench step (channel-last prefill,
+// channel-first prefill, decode, paged) 4% slower on GB300, while launches
+// of the same kernel back to back gained nothing from it (measured).  The
+// short kernels, one wave each, release at once.
+#include <cstdlib>
+#include <cstring>
 #include <type_traits>
 #include <utility>
 
@@ -132,11 +146,12 @@ __device__ __forceinline__ void stage_weights(const uint16_t *w, int64_t ws_d, i
     __syncthreads();
 }
 
-// The blocks of chunk slot i < batch and the first channel tile each check
-// sequence i's indices and count invalid ones; the chunk blocks skip such
-// sequences silently.  validate_sequence: slot blockIdx.x, tile blockIdx.y.
+// One thread of the work unit (block or warp) of chunk slot i < batch in
+// the first channel tile checks sequence i's indices and counts invalid
+// ones; the chunk units skip such sequences silently.  validate_sequence:
+// slot blockIdx.x, tile blockIdx.y, thread 0.
 __device__ __forceinline__ void validate_sequence_at(const FwdArgs &a, int i, bool lead) {
-    if (a.err == nullptr || !lead || threadIdx.x != 0) return;
+    if (a.err == nullptr || !lead) return;
     if (i >= a.batch) return;
     const int line = a.cidx ? __ldg(a.cidx + i) : i;
     if (line == a.pad) return;
@@ -146,7 +161,7 @@ __device__ __forceinline__ void validate_sequence_at(const FwdArgs &a, int i, bo
     if (bad) atomicAdd(a.err, 1);
 }
 __device__ __forceinline__ void validate_sequence(const FwdArgs &a) {
-    validate_sequence_at(a, blockIdx.x, blockIdx.y == 0);
+    validate_sequence_at(a, blockIdx.x, blockIdx.y == 0 && threadIdx.x == 0);
 }
 
 // Resolve the state line of the chunk's sequence; false = skip the sequence.
@@ -215,8 +230,7 @@ __global__ void __launch_bounds__(kThreads) fwd_cl_kernel(const FwdArgs a) {
     constexpr int TILE_C = 32 * VEC;
     __shared__ __align__(16) uint16_t s_w[W * TILE_C];
     __shared__ __align__(16) uint16_t s_b[TILE_C];
-    release_next_grid();
-    wait_prior_grid();
+    wait_prior_grid();  // no early release: see the note on the streaming kernels' launches
     validate_sequence(a);
     ChunkInfo ci;
     if (!locate_chunk(a, kClChunk, blockIdx.x, ci)) return;
@@ -309,8 +323,7 @@ template <int W, bool SILU, int VEC>
 __global__ void __launch_bounds__(kThreads) fwd_cf_kernel(const FwdArgs a) {
     constexpr int SEG = 32 * VEC;
     constexpr int CHUNK = kCfSegs * SEG;
-    release_next_grid();
-    wait_prior_grid();
+    wait_prior_grid();  // no early release: see the note on the streaming kernels' launches
     validate_sequence(a);
     ChunkInfo ci;
     if (!locate_chunk(a, CHUNK, blockIdx.x, ci)) return;
@@ -518,15 +531,14 @@ __global__ void __launch_bounds__(kCaThreads, W == 5 ? 2 : 3) fwd_cl_async_kerne
     extern __shared__ __align__(16) uint4 s_ring[];  // [kCaSlots][kCaThreads]
     __shared__ __align__(16) uint16_t s_w[W * kCaTileC];
     __shared__ __align__(16) uint16_t s_b[kCaTileC];
-    release_next_grid();
-    wait_prior_grid();
+    wait_prior_grid();  // no early release: see the note on the streaming kernels' launches
     // One-dimensional grid, block = slot * tiles + tile: channel tiles vary
     // fastest in launch order, so the blocks resident at one time read whole
     // token rows (3% faster than chunk-major order, measured).
     const int ntiles = (a.dim + kCaTileC - 1) / kCaTileC;
     const int tile = static_cast<int>(blockIdx.x % static_cast<unsigned>(ntiles));
     const int slot = static_cast<int>(blockIdx.x / static_cast<unsigned>(ntiles));
-    validate_sequence_at(a, slot, tile == 0);
+    validate_sequence_at(a, slot, tile == 0 && threadIdx.x == 0);
     ChunkInfo ci;
     if (!locate_chunk(a, kCaChunk, slot, ci)) return;
 
@@ -748,8 +760,7 @@ __device__ __forceinline__ uint4 cfa_outputs(const uint32_t (&E)[6], const uint3
 template <int W, bool SILU>
 __global__ void __launch_bounds__(kCfaThreads, 4) fwd_cf_async_kernel(const FwdArgs a) {
     extern __shared__ __align__(16) uint4 s_ring[];  // [kCfaSlots][kCfaThreads]
-    release_next_grid();
-    wait_prior_grid();
+    wait_prior_grid();  // no early release: see the note on the streaming kernels' launches
     validate_sequence(a);
     ChunkInfo ci;
     if (!locate_chunk(a, kCfaChunk, blockIdx.x, ci)) return;
@@ -933,6 +944,293 @@ __global__ void __launch_bounds__(kCfaThreads, 4) fwd_cf_async_kernel(const FwdA
     }
 }
 
+// ------------------------------------------------------ short problems ----
+//
+// A problem too small to fill the machine with streaming chunks is set by
+// latency, not bandwidth: the dependent round trips before the first store
+// (sequence search, state line, state columns, inputs) and the ring
+// prologue.  These kernels cut that chain to two round trips for up to 32
+// sequences.  A warp owns one short chunk of one sequence and one channel
+// tile (channel-last) or channel row (channel-first); its lanes look up the
+// chunk's sequence together with every candidate's end, state line and
+// has_initial_state flag in one round trip, then load the chunk's inputs
+// and the state columns straight into registers and compute.
+
+constexpr int kShortThreads = 128;
+constexpr int kShortWarps = kShortThreads / 32;
+constexpr int kShortRun = 8;  // channel-last: tokens per warp (one run)
+constexpr int kShortSegs = 2;  // channel-first: 256-token segments per warp
+// channel-first chunk: a window of kShortSegs * 256 tokens that starts on the
+// 16-byte boundary at or before the chunk's first token covers it
+constexpr int kShortCfChunk = kShortSegs * 256 - 8;
+
+struct ShortChunk {
+    int seq, chunk, start, len, line;
+    bool init;
+};
+
+// Slot -> (sequence, chunk) as locate_chunk, plus the sequence's state line
+// and has_initial_state flag: lane j of the final round loads candidate j's
+// offsets, line and flag together, and the winner's are shuffled to every
+// lane.  false for a surplus slot, a pad or invalid line, or bad offsets.
+__device__ __forceinline__ bool locate_short(const FwdArgs &a, int chunk_tokens, int slot,
+                                             ShortChunk &sc) {
+    const int lane = threadIdx.x & 31;
+    int lo = 0, n = a.batch;
+    while (n > 32) {  // narrow to at most 32 candidates
+        const int stride = (n + 31) >> 5;
+        const int off = lane * stride;
+        bool le = false;
+        if (off < n) {
+            const int i = lo + off;
+            le = floor_div(__ldg(a.qsl + i), chunk_tokens) + i <= slot;
+        }
+        const unsigned m = __ballot_sync(kFullMask, le);
+        if (m == 0u) return false;
+        const int top = 31 - __clz(m);
+        lo += top * stride;
+        n = min(stride, n - top * stride);
+    }
+    int s = 0, e = 0, line = 0, init = 0;
+    bool le = false;
+    if (lane < n) {
+        const int i = lo + lane;
+        s = __ldg(a.qsl + i);
+        e = __ldg(a.qsl + i + 1);
+        line = a.cidx ? __ldg(a.cidx + i) : i;
+        init = a.has_init != nullptr ? a.has_init[i] : 0;
+        le = floor_div(s, chunk_tokens) + i <= slot;
+    }
+    const unsigned m = __ballot_sync(kFullMask, le);
+    if (m == 0u) return false;
+    const int top = 31 - __clz(m);
+    sc.seq = lo + top;
+    sc.start = __shfl_sync(kFullMask, s, top);
+    const int end = __shfl_sync(kFullMask, e, top);
+    sc.line = __shfl_sync(kFullMask, line, top);
+    sc.init = a.st != nullptr && __shfl_sync(kFullMask, init, top) != 0;
+    if (sc.start < 0 || end < sc.start || end > a.total) return false;
+    const int k = slot - (sc.start / chunk_tokens + sc.seq);
+    if (k < 0 || static_cast<int64_t>(k) * chunk_tokens >= end - sc.start) return false;
+    if (sc.line == a.pad) return false;
+    if (a.st != nullptr && (sc.line < 0 || sc.line >= a.num_lines)) return false;
+    sc.chunk = k;
+    sc.len = end - sc.start;
+    return true;
+}
+
+// Channel-last: warp = (run of kShortRun tokens, 256-channel tile), lane =
+// 8 channels; global warp g = slot * tiles + tile.
+template <int W, bool SILU>
+__global__ void __launch_bounds__(kShortThreads) fwd_cl_short_kernel(const FwdArgs a, int nslots) {
+    release_next_grid();
+    wait_prior_grid();
+    const int lane = threadIdx.x & 31;
+    const int ntiles = (a.dim + 255) / 256;
+    const int g = blockIdx.x * kShortWarps + (threadIdx.x >> 5);
+    const int tile = g % ntiles;
+    const int slot = g / ntiles;
+    if (slot >= nslots) return;  // warp-uniform
+    validate_sequence_at(a, slot, tile == 0 && lane == 0);
+    ShortChunk sc;
+    if (!locate_short(a, kShortRun, slot, sc)) return;
+    const int c0 = tile * 256 + lane * 8;
+    if (c0 >= a.dim) return;
+
+    const int64_t xs = a.xs_t;
+    const uint16_t *xc = a.x + c0;
+    const int r0 = sc.start + sc.chunk * kShortRun;
+    const int n = min(kShortRun, sc.len - sc.chunk * kShortRun);
+    const bool first = sc.chunk == 0;
+    // Every load of the chunk goes out at once: its rows, the W-1 inputs
+    // before it (x rows, or the state columns for a sequence's first run)
+    // and, for the first run, the rows the new state takes from x.
+    uint4 v[kShortRun];
+#pragma unroll
+    for (int m = 0; m < kShortRun; ++m)
+        v[m] = m < n ? __ldg(reinterpret_cast<const uint4 *>(xc + (r0 + m) * xs)) : make_uint4(0u, 0u, 0u, 0u);
+    uint4 ring[W - 1];
+#pragma unroll
+    for (int j = 0; j < W - 1; ++j) {
+        ring[j] = make_uint4(0u, 0u, 0u, 0u);
+        if (!first) ring[j] = *reinterpret_cast<const uint4 *>(xc + (r0 - (W - 1) + j) * xs);
+        else if (sc.init) ring[j] = load8_state(a, sc.line, c0, j);
+    }
+    uint4 nw[W - 1];
+    const bool write_state = first && a.st != nullptr;
+    if (write_state) {
+        // New state = last W-1 entries of prior ++ x[sequence].
+#pragma unroll
+        for (int j = 0; j < W - 1; ++j) {
+            const int idx = sc.len + j;
+            if (idx < W - 1) {
+#pragma unroll
+                for (int q = 0; q < W - 1; ++q)
+                    if (q == idx) nw[j] = ring[q];
+            } else {
+                nw[j] = *reinterpret_cast<const uint4 *>(xc + (sc.start + idx - (W - 1)) * xs);
+            }
+        }
+    }
+    uint4 wpk[W];
+    const bool w_vec = a.ws_k == 1 && a.ws_d == W && (reinterpret_cast<uintptr_t>(a.w) & 15u) == 0;
+    load_weights8<W>(a.w, a.ws_d, a.ws_k, c0, a.dim, w_vec, wpk);
+    float bs[8];
+    load_bias8(a.bias, c0, a.dim, (reinterpret_cast<uintptr_t>(a.bias) & 15u) == 0, bs);
+
+    uint16_t *dst = a.out + c0 + static_cast<int64_t>(r0) * a.os_t;
+#pragma unroll
+    for (int m = 0; m < kShortRun; ++m) {
+        if (m >= n) break;
+        __stcs(reinterpret_cast<uint4 *>(dst), ca_row<W, SILU>(wpk, bs, ring, v[m]));
+        dst += a.os_t;
+#pragma unroll
+        for (int k = 0; k < W - 2; ++k) ring[k] = ring[k + 1];
+        ring[W - 2] = v[m];
+    }
+    if (write_state) {
+#pragma unroll
+        for (int j = 0; j < W - 1; ++j) store8_state(a, sc.line, c0, j, nw[j]);
+    }
+}
+
+// The 8 logical inputs at tokens t0..t0+7 of one channel-first row, from
+// `raw` (those tokens as loaded where they lie inside [0, total), else 0):
+// x inside [lo, cend), the prior (packed, oldest first) just before a
+// sequence's first chunk, 0 elsewhere.
+template <int W>
+__device__ __forceinline__ uint4 short_mask(uint4 raw, int t0, int lo, int cbeg, int cend, bool chunk0,
+                                            uint32_t prior01, uint32_t prior23) {
+    if (t0 >= lo && t0 + 8 <= cend) return raw;
+    uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t pair = 0;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int t = t0 + 2 * q + e;
+            uint32_t val = 0;
+            if (t >= lo && t < cend) {
+                val = e ? (w[q] >> 16) : (w[q] & 0xffffu);
+            } else if (chunk0 && t >= cbeg - (W - 1) && t < cbeg) {
+                const int i = t - cbeg + (W - 1);  // prior column
+                const uint32_t src = i < 2 ? prior01 : prior23;
+                val = (i & 1) ? (src >> 16) : (src & 0xffffu);
+            }
+            pair |= val << (16 * e);
+        }
+        w[q] = pair;
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Tokens t0..t0+7 of row xc as loaded: one 16-byte load when all lie inside
+// [0, total) (t0 is on a 16-byte boundary), else element by element.
+__device__ __forceinline__ uint4 short_load(const uint16_t *xc, int t0, int total) {
+    if (t0 >= 0 && t0 + 8 <= total) return __ldg(reinterpret_cast<const uint4 *>(xc + t0));
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int t = t0 + 2 * q;
+        const uint32_t lo = t >= 0 && t < total ? xc[t] : 0u;
+        const uint32_t hi = t + 1 >= 0 && t + 1 < total ? xc[t + 1] : 0u;
+        w[q] = lo | (hi << 16);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Channel-first: warp = (chunk of kShortCfChunk tokens, channel row), as
+// kShortSegs segments of 256 tokens from the 16-byte boundary at or before
+// the chunk's first token; lane l owns tokens 8l..8l+7 of each segment, and
+// the W-1 tokens before them come from lane l-1 by shuffle (lane 0: lane 31
+// of the segment before, or the vector before the window).
+template <int W, bool SILU>
+__global__ void __launch_bounds__(kShortThreads) fwd_cf_short_kernel(const FwdArgs a) {
+    release_next_grid();
+    wait_prior_grid();
+    const int lane = threadIdx.x & 31;
+    const int slot = blockIdx.x;
+    const int c = blockIdx.y * kShortWarps + (threadIdx.x >> 5);
+    validate_sequence_at(a, slot, blockIdx.y == 0 && threadIdx.x == 0);
+    if (c >= a.dim) return;  // warp-uniform
+    ShortChunk sc;
+    if (!locate_short(a, kShortCfChunk, slot, sc)) return;
+
+    const uint16_t *const xc = a.x + c * a.xs_d;
+    const int cbeg = sc.start + sc.chunk * kShortCfChunk;
+    const int cend = sc.start + min(sc.len, (sc.chunk + 1) * kShortCfChunk);
+    const bool chunk0 = sc.chunk == 0;
+    const int lo = chunk0 ? cbeg : cbeg - (W - 1);
+    const int phase = static_cast<int>((reinterpret_cast<uintptr_t>(xc) >> 1) & 7u);
+    const int a0 = cbeg - ((phase + cbeg) & 7);  // on a 16-byte boundary, a0 > cbeg - 8
+    // Every load goes out at once: the window's vectors, the vector before
+    // it (lane 0), the state columns and the inputs the new state takes.
+    uint4 raw[kShortSegs];
+#pragma unroll
+    for (int sg = 0; sg < kShortSegs; ++sg) raw[sg] = short_load(xc, a0 + sg * 256 + lane * 8, a.total);
+    uint4 raw_before = make_uint4(0u, 0u, 0u, 0u);
+    if (lane == 0) raw_before = short_load(xc, a0 - 8, a.total);
+    uint32_t p[4] = {0, 0, 0, 0};
+    if (chunk0 && sc.init) {
+        const uint16_t *sp = a.st + sc.line * a.ss_l + c * a.ss_d;
+#pragma unroll
+        for (int j = 0; j < W - 1; ++j) p[j] = sp[j * a.ss_t];
+    }
+    const bool write_state = chunk0 && a.st != nullptr;
+    uint32_t from_x = 0;  // the new state's column `lane` when it comes from x
+    const int idx = sc.len + lane;
+    if (write_state && lane < W - 1 && idx >= W - 1) from_x = xc[sc.start + idx - (W - 1)];
+    uint32_t wt[W];  // tap k's bf16 weight in both halves
+#pragma unroll
+    for (int k = 0; k < W; ++k) wt[k] = 0x10001u * __ldg(a.w + c * a.ws_d + k * a.ws_k);
+    const float bs = a.bias ? bf16_bits(__ldg(a.bias + c)) : 0.0f;
+
+    const uint32_t prior01 = p[0] | (p[1] << 16), prior23 = p[2] | (p[3] << 16);
+    const uint4 before = short_mask<W>(raw_before, a0 - 8, lo, cbeg, cend, chunk0, prior01, prior23);
+    uint32_t prev_z = before.z, prev_w = before.w;  // tokens a0-4 .. a0-1 (lane 0)
+    uint16_t *const oc = a.out + c * a.os_d;
+#pragma unroll
+    for (int sg = 0; sg < kShortSegs; ++sg) {
+        const int t0 = a0 + sg * 256 + lane * 8;
+        const uint4 v = short_mask<W>(raw[sg], t0, lo, cbeg, cend, chunk0, prior01, prior23);
+        const uint32_t up_z = __shfl_up_sync(kFullMask, v.z, 1);
+        const uint32_t up_w = __shfl_up_sync(kFullMask, v.w, 1);
+        const uint32_t pv_z = __shfl_sync(kFullMask, prev_z, sg == 0 ? 0 : 31);
+        const uint32_t pv_w = __shfl_sync(kFullMask, prev_w, sg == 0 ? 0 : 31);
+        prev_z = v.z;
+        prev_w = v.w;
+        const uint32_t E[6] = {lane ? up_z : pv_z, lane ? up_w : pv_w, v.x, v.y, v.z, v.w};
+        if (t0 + 8 <= cbeg || t0 >= cend) continue;
+        const uint4 o = cfa_outputs<W, SILU>(E, wt, bs);
+        if (t0 >= cbeg && t0 + 8 <= cend) {
+            __stcs(reinterpret_cast<uint4 *>(oc + t0), o);
+        } else {
+            const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int t = t0 + i;
+                if (t >= cbeg && t < cend)
+                    oc[t] = uint16_t((i & 1) ? (ow[i >> 1] >> 16) : (ow[i >> 1] & 0xffffu));
+            }
+        }
+    }
+    if (write_state) {
+        // New state = last W-1 entries of prior ++ x[sequence]; every lane
+        // read the prior above, before any lane writes the line.
+        uint16_t nb = 0;
+        if (lane < W - 1) {
+            if (idx < W - 1) {
+                const uint32_t src = idx < 2 ? prior01 : prior23;
+                nb = uint16_t((idx & 1) ? (src >> 16) : (src & 0xffffu));
+            } else {
+                nb = uint16_t(from_x);
+            }
+        }
+        __syncwarp();
+        if (lane < W - 1) a.st[sc.line * a.ss_l + c * a.ss_d + lane * a.ss_t] = nb;
+    }
+}
+
 // ----------------------------------------------------------- dispatch ----
 
 using KernelFn = void (*)(FwdArgs);
@@ -978,6 +1276,57 @@ int launch_cf_async_w(const FwdArgs &a, cudaStream_t stream) {
                     static_cast<unsigned>((a.dim + kCfaWarps - 1) / kCfaWarps));
     if (grid.y > 65535u) return CCV_ERR_SIZE;
     return launch_pdl(fwd_cf_async_kernel<W, SILU>, grid, dim3(kCfaThreads), kCfaSmem, stream, a);
+}
+
+template <int W, bool SILU>
+int launch_cl_short_w(const FwdArgs &a, cudaStream_t stream) {
+    const int64_t nslots = static_cast<int64_t>(a.total) / kShortRun + a.batch;
+    const int64_t warps = nslots * ((a.dim + 255) / 256);
+    const int64_t blocks = (warps + kShortWarps - 1) / kShortWarps;
+    if (nslots > 0x7fffffff || blocks > 0x7fffffff) return CCV_ERR_SIZE;
+    return launch_pdl(fwd_cl_short_kernel<W, SILU>, dim3(static_cast<unsigned>(blocks)),
+                      dim3(kShortThreads), 0, stream, a, static_cast<int>(nslots));
+}
+
+template <int W, bool SILU>
+int launch_cf_short_w(const FwdArgs &a, cudaStream_t stream) {
+    const int64_t nslots = static_cast<int64_t>(a.total) / kShortCfChunk + a.batch;
+    const dim3 grid(static_cast<unsigned>(nslots),
+                    static_cast<unsigned>((a.dim + kShortWarps - 1) / kShortWarps));
+    return launch_pdl(fwd_cf_short_kernel<W, SILU>, grid, dim3(kShortThreads), 0, stream, a);
+}
+
+int launch_cl_short(const FwdArgs &a, int width, bool silu, cudaStream_t stream) {
+    switch (width) {
+        case 2: return silu ? launch_cl_short_w<2, true>(a, stream) : launch_cl_short_w<2, false>(a, stream);
+        case 3: return silu ? launch_cl_short_w<3, true>(a, stream) : launch_cl_short_w<3, false>(a, stream);
+        case 4: return silu ? launch_cl_short_w<4, true>(a, stream) : launch_cl_short_w<4, false>(a, stream);
+        case 5: return silu ? launch_cl_short_w<5, true>(a, stream) : launch_cl_short_w<5, false>(a, stream);
+    }
+    return CCV_ERR_WIDTH;
+}
+
+int launch_cf_short(const FwdArgs &a, int width, bool silu, cudaStream_t stream) {
+    switch (width) {
+        case 2: return silu ? launch_cf_short_w<2, true>(a, stream) : launch_cf_short_w<2, false>(a, stream);
+        case 3: return silu ? launch_cf_short_w<3, true>(a, stream) : launch_cf_short_w<3, false>(a, stream);
+        case 4: return silu ? launch_cf_short_w<4, true>(a, stream) : launch_cf_short_w<4, false>(a, stream);
+        case 5: return silu ? launch_cf_short_w<5, true>(a, stream) : launch_cf_short_w<5, false>(a, stream);
+    }
+    return CCV_ERR_WIDTH;
+}
+
+// Which prefill kernels serve a problem of `elems` = total_tokens * dim
+// elements: the short kernels up to kShortMaxElems, the streaming kernels
+// above.  The environment variable CCV_PREFILL_PATH=short or =stream forces
+// one family (both compute the same results; for tests and tuning).
+constexpr int64_t kShortMaxElems = int64_t(1) << 23;
+
+bool use_short_path(int64_t elems) {
+    const char *force = std::getenv("CCV_PREFILL_PATH");
+    if (force != nullptr && std::strcmp(force, "short") == 0) return true;
+    if (force != nullptr && std::strcmp(force, "stream") == 0) return false;
+    return elems <= kShortMaxElems;
 }
 
 int launch_cl_async(const FwdArgs &a, int width, bool silu, cudaStream_t stream) {
@@ -1064,7 +1413,11 @@ extern "C" int ccv_fwd(const void *x, int64_t x_stride_dim, int64_t x_stride_tok
         const bool vec = dim % 8 == 0 && aligned16(x) && aligned16(out) && tok_ok;
         a.st_vec = vec && conv_states != nullptr && s_stride_dim == 1 && aligned16(conv_states) &&
                    s_stride_line % 8 == 0 && s_stride_tok % 8 == 0;
-        if (vec) return launch_cl_async(a, width, is_silu, stream);
+        if (vec) {
+            return use_short_path(static_cast<int64_t>(total_tokens) * dim)
+                       ? launch_cl_short(a, width, is_silu, stream)
+                       : launch_cl_async(a, width, is_silu, stream);
+        }
         fn = pick_kernel<1, true>(width, is_silu);
         grid = dim3(static_cast<unsigned>(total_tokens / kClChunk + batch),
                     static_cast<unsigned>((dim + 31) / 32));
@@ -1074,7 +1427,12 @@ extern "C" int ccv_fwd(const void *x, int64_t x_stride_dim, int64_t x_stride_tok
         const bool same_phase = (reinterpret_cast<uintptr_t>(x) & 1u) == 0 &&
                                 (reinterpret_cast<uintptr_t>(out) & 1u) == 0 && xo == oo &&
                                 (x_stride_dim - out_stride_dim) % 8 == 0;
-        if (same_phase) return launch_cf_async(a, width, is_silu, stream);
+        if (same_phase) {
+            const bool fits = (dim + kShortWarps - 1) / kShortWarps <= 65535;
+            return fits && use_short_path(static_cast<int64_t>(total_tokens) * dim)
+                       ? launch_cf_short(a, width, is_silu, stream)
+                       : launch_cf_async(a, width, is_silu, stream);
+        }
         fn = pick_kernel<1, false>(width, is_silu);
         grid = dim3(static_cast<unsigned>(total_tokens / (kCfSegs * 32) + batch),
                     static_cast<unsigned>((dim + kWarps - 1) / kWarps));

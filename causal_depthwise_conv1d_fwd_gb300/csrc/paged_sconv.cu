@@ -245,26 +245,38 @@ __global__ void __launch_bounds__(kThreads) paged_scalar_kernel(const PagedArgs 
     }
 }
 
-// Vector kernel: a lane owns 8 channels (16 bytes) and a warp a run of
-// kVecRun tokens.  The warp stages its x rows (the W-1 before the run, then
-// the run) in shared memory with per-lane asynchronous copies; each lane
-// reads back only the slots it filled, so its own wait is the only
-// synchronisation.  When every token of the run takes all W taps from x (an
-// interior stretch of a prefill, the usual case), a straight loop keeps the
-// taps in a register ring of raw bf16 rows and shuffles only the insert
-// offset; otherwise each token follows its plan (x rows from shared memory,
-// cache taps from global memory).  Taps are native bf16 x bf16 + fp32 FMAs
-// on packed weights.  Short runs and a register bound of 7 blocks per SM
-// keep enough warps in flight: the work is latency-bound, not
-// bandwidth-bound, at serving batch sizes.
-constexpr int kVecRun = 8;
-constexpr int kStageGroup = 4;  // staged rows per asynchronous-copy group
-constexpr int kVecBlockTokens = kWarps * kVecRun;
-constexpr int kVecChannels = 32 * 8;
+// Row kernel: a block covers a run of kRowRun tokens across up to
+// kRowMaxThreads * 8 channels -- every channel of a 2048-channel stream --
+// with a thread per 8 consecutive channels (one 16-byte vector, all in one
+// head because ws is a multiple of 8).  Each thread first streams its x
+// vectors of the run and of the W-1 rows before it into a private ring of
+// shared-memory slots with asynchronous copies (it reads back only its own
+// slots, so its own wait is the only synchronisation for them).  Meanwhile
+// the first warp resolves every token's plan once -- the four index loads,
+// then the block-table lookups of its pre-forward taps -- into shared
+// memory, and one barrier publishes it to the block.  When every token of
+// the run takes all W taps from x and has an insert slot (an interior
+// stretch of a prefill, the usual case) a straight loop keeps the taps in a
+// register ring of raw bf16 rows; otherwise each token follows its plan (x
+// rows from the ring, cache taps from global memory).  Taps are native bf16
+// x bf16 + fp32 FMAs on packed weights; the residual enters the same way
+// (x * 1 + act, one rounding).
+constexpr int kRowRun = 8;           // tokens per block (at most 32: one planning lane each)
+constexpr int kRowMaxThreads = 256;  // 2048 channels per block
+constexpr int kStageGroup = 4;       // staged rows per asynchronous-copy group
+
+// One run's plans, written by the first warp and read by every thread.
+template <int W>
+struct RunPlan {
+    int64_t ins[kRowRun];
+    int64_t off[kRowRun][W];
+    int kinds[kRowRun];
+    int all_x;
+};
 
 template <int W>
-constexpr int vec_smem_bytes() {
-    return kWarps * (kVecRun + W - 1) * 32 * 16;
+constexpr int row_slots() {
+    return kRowRun + W - 1;
 }
 
 template <int W>
@@ -278,17 +290,20 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &v, int q) {
     return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
 }
 
-// SiLU, then the residual (x of the token, widened exactly), then bf16
-// rounding of one lane's 8 outputs.
+constexpr uint32_t kBf16OnePair = 0x3f803f80u;  // (1.0, 1.0) as bf16x2
+
+// SiLU, then the residual (x of the token times 1 plus the activation: one
+// rounding, the same value as the fp32 sum), then bf16 rounding of one
+// thread's 8 outputs.
 template <bool SILU, bool RESID>
-__device__ __forceinline__ uint4 finish_row(const float (&acc)[8], const uint4 &xr) {
+__device__ __forceinline__ uint4 finish_row(float (&acc)[8], const uint4 &xr) {
     uint32_t o[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        f32x2 r = pack2(acc[2 * q], acc[2 * q + 1]);
-        if (SILU) r = silu2(r);
-        if (RESID) r = add2(r, widen2(word_of(xr, q)));
-        o[q] = f32x2_to_bf16x2(r);
+        float lo = acc[2 * q], hi = acc[2 * q + 1];
+        if (SILU) unpack2(silu2(pack2(lo, hi)), lo, hi);
+        if (RESID) fma_bf16x2(lo, hi, word_of(xr, q), kBf16OnePair);
+        o[q] = f32x2_to_bf16x2(pack2(lo, hi));
     }
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
@@ -312,11 +327,12 @@ __device__ __forceinline__ uint4 paged_row(const uint4 (&wpk)[W], const uint4 (&
 }
 
 template <int W, bool SILU, bool RESID>
-__global__ void __launch_bounds__(kThreads, 7) paged_vec_kernel(const PagedLaunch pl) {
-    extern __shared__ uint4 stage[];
+__global__ void __launch_bounds__(kRowMaxThreads, 4) paged_row_kernel(const PagedLaunch pl) {
+    extern __shared__ uint4 stage[];  // [row_slots<W>()][blockDim.x]
+    __shared__ RunPlan<W> plan;
+    constexpr int R = row_slots<W>();
     release_next_grid();
     wait_prior_grid();
-    constexpr int R = kVecRun + W - 1;
     PagedArgs a = pl.a;
     if (gridDim.z > 1) {
         // constant indices only: no dynamic indexing into the parameters
@@ -331,59 +347,66 @@ __global__ void __launch_bounds__(kThreads, 7) paged_vec_kernel(const PagedLaunc
             default: apply_stream(a, pl.s[7]); break;
         }
     }
-    if (blockIdx.y * kVecChannels >= a.C) return;  // this stream has fewer channel tiles
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    const int t0 = blockIdx.x * kVecBlockTokens + warp * kVecRun;
-    const int t1 = min(t0 + kVecRun, a.T);
-    if (t0 >= t1) return;  // warp-uniform
-    const int c0 = blockIdx.y * kVecChannels + lane * 8;
-    const bool active = c0 < a.C;  // inactive lanes still take part in the shuffles
-    uint4 *xs = stage + warp * R * 32 + lane;  // row m of the warp's window at xs[m * 32]
+    const int nthreads = blockDim.x;
+    const int tile_c = nthreads * 8;
+    if (static_cast<int>(blockIdx.y) * tile_c >= a.C) return;  // block-uniform: this stream is narrower
+    const int tid = threadIdx.x;
+    const int t0 = blockIdx.x * kRowRun;
+    const int n = min(kRowRun, a.T - t0);  // >= 1: the grid covers T exactly
+    const int c0 = blockIdx.y * tile_c + tid * 8;
+    const bool active = c0 < a.C;
+    uint4 *xs = stage + tid;  // row m of the run's window at xs[m * nthreads]
 
-    // Every load that does not depend on another goes out first -- weights,
-    // the lane's token indices, then the staged x rows -- so a warp waits for
-    // one memory round trip before the block-table lookups, not three.
-    uint4 wpk[W];
-    load_weights8<W>(a.w, a.ws_c, a.ws_k, active ? c0 : 0, a.C, a.w_vec, wpk);
-    const TokenMeta meta = load_meta(a, t0 + lane, t0 + lane < t1);
+    // The x stream goes out first: rows t0-(W-1) .. t0+n-1, in commit groups
+    // of kStageGroup rows so the straight loop can start on the first ones.
 #pragma unroll
     for (int m = 0; m < R; ++m) {
         const int row = t0 - (W - 1) + m;
-        if (active && row >= 0 && row < t1) cp_async16(xs + m * 32, a.x + row * a.xs_t + c0);
-        else xs[m * 32] = make_uint4(0u, 0u, 0u, 0u);
+        if (active && row >= 0 && row < t0 + n) cp_async16(xs + m * nthreads, a.x + row * a.xs_t + c0);
+        else xs[m * nthreads] = make_uint4(0u, 0u, 0u, 0u);
         if (m % kStageGroup == kStageGroup - 1 || m == R - 1) cp_async_commit();
     }
+    uint4 wpk[W];
+    load_weights8<W>(a.w, a.ws_c, a.ws_k, active ? c0 : 0, a.C, a.w_vec, wpk);
+    if (tid < 32) {
+        // Lane u plans token t0 + u; lanes past the run carry an empty plan.
+        const TokenPlan<W> p = plan_token<W>(a, t0 + tid, load_meta(a, t0 + tid, tid < n));
+        if (tid < kRowRun) {
+            plan.kinds[tid] = p.kinds;
+            plan.ins[tid] = p.ins;
+#pragma unroll
+            for (int iw = 0; iw < W; ++iw) plan.off[tid][iw] = p.off[iw];
+        }
+        const bool ax = __all_sync(kFullMask, tid >= n || (p.kinds == all_x_kinds<W>() && p.ins >= 0));
+        if (tid == 0) plan.all_x = ax;
+    }
+    __syncthreads();
+    if (!active) return;  // no copies were issued for an inactive thread
 
-    const TokenPlan<W> mine = plan_token<W>(a, t0 + lane, meta);
-    const bool all_x = __all_sync(kFullMask, t0 + lane >= t1 ||
-                                                 (mine.kinds == all_x_kinds<W>() && mine.ins >= 0));
+    const int head = c0 / a.ws;
+    const int64_t chan_off = static_cast<int64_t>(head) * a.cs_h + a.off_s + c0 % a.ws;
+    uint16_t *op = a.out + static_cast<int64_t>(t0) * a.os_t + c0;
 
-    const int head = active ? c0 / a.ws : 0;
-    const int64_t chan_off = static_cast<int64_t>(head) * a.cs_h + a.off_s + (active ? c0 % a.ws : 0);
-    const int n = t1 - t0;
-
-    if (all_x) {
+    if (plan.all_x) {
         // Token u needs staged rows up to u + W - 1: wait only for the copy
         // groups up to that row, so stores start while later rows arrive.
         constexpr int kGroups = (R + kStageGroup - 1) / kStageGroup;
         uint4 ring[W - 1];
         cp_async_wait<kGroups - 1 - (W - 1) / kStageGroup>();  // rows 0 .. W-1
 #pragma unroll
-        for (int m = 0; m < W - 1; ++m) ring[m] = xs[m * 32];
+        for (int m = 0; m < W - 1; ++m) ring[m] = xs[m * nthreads];
 #pragma unroll
-        for (int u = 0; u < kVecRun; ++u) {
-            if (u >= n) break;  // warp-uniform
+        for (int u = 0; u < kRowRun; ++u) {
+            if (u >= n) break;  // block-uniform
             // Wait only where the needed group changes: a wait orders all
             // memory accesses around it, so tokens between two waits can
             // still be interleaved by the compiler.
             const int need = (u + W - 1) / kStageGroup;
             if (u > 0 && need != (u + W - 2) / kStageGroup) cp_async_wait_upto(kGroups - 1 - need);
-            const int64_t ins = shfl64(mine.ins, u);
-            const uint4 xr = xs[(u + W - 1) * 32];
-            if (active) *reinterpret_cast<uint4 *>(a.cache + ins + chan_off) = xr;
-            const uint4 o = paged_row<W, SILU, RESID>(wpk, ring, xr);
-            if (active) __stcs(reinterpret_cast<uint4 *>(a.out + (t0 + u) * a.os_t + c0), o);
+            const uint4 xr = xs[(u + W - 1) * nthreads];
+            *reinterpret_cast<uint4 *>(a.cache + plan.ins[u] + chan_off) = xr;
+            __stcs(reinterpret_cast<uint4 *>(op), paged_row<W, SILU, RESID>(wpk, ring, xr));
+            op += a.os_t;
 #pragma unroll
             for (int m = 0; m < W - 2; ++m) ring[m] = ring[m + 1];
             ring[W - 2] = xr;
@@ -391,92 +414,54 @@ __global__ void __launch_bounds__(kThreads, 7) paged_vec_kernel(const PagedLaunc
         return;
     }
 
-    // General path.  The cache taps of a group of tokens are loaded before
-    // any of the group's stores, so their latencies overlap instead of
-    // queueing behind the stores (which the compiler cannot prove disjoint).
-    constexpr int kGroup = W <= 3 ? 4 : 2;  // at most 8 vectors of taps in flight
-    // First pull every cache tap of the run into L1: prefetches hold no
-    // registers, so the whole run's round trip overlaps, and the grouped
-    // loads below hit L1.  Pre-forward positions are never written in this
-    // launch, so their lines in L1 stay valid.
+    // General path.  First pull every cache tap of the run into L1:
+    // prefetches hold no registers, so the whole run's round trip overlaps,
+    // and the grouped loads below hit L1.  Pre-forward positions are never
+    // written in this launch, so their lines in L1 stay valid.
 #pragma unroll 1
     for (int u = 0; u < n; ++u) {
-        const int kinds = __shfl_sync(kFullMask, mine.kinds, u);
+        const int kinds = plan.kinds[u];
 #pragma unroll
-        for (int iw = 0; iw < W; ++iw) {
-            const int64_t off = shfl64(mine.off[iw], u);
-            if (active && ((kinds >> (2 * iw)) & 3) == kTapCache) prefetch_l1(a.cache + off + chan_off);
-        }
+        for (int iw = 0; iw < W; ++iw)
+            if (((kinds >> (2 * iw)) & 3) == kTapCache) prefetch_l1(a.cache + plan.off[u][iw] + chan_off);
     }
     cp_async_wait<0>();
 #pragma unroll 1
-    for (int g = 0; g < n; g += kGroup) {
-        uint4 cached[kGroup][W - 1];
+    for (int u = 0; u < n; ++u) {
+        const int kinds = plan.kinds[u];
+        const int64_t ins = plan.ins[u];
+        const uint4 xr = xs[(u + W - 1) * nthreads];
+        // The taps are read before the insert is written: the compiler cannot
+        // prove them disjoint, and a read after the store would wait for it.
+        uint4 tap[W];
 #pragma unroll
-        for (int j = 0; j < kGroup; ++j) {
-            // g + j < 8 + 4 <= 32; lanes without a token carry an empty plan.
-            const int kinds = __shfl_sync(kFullMask, mine.kinds, g + j);
-#pragma unroll
-            for (int iw = 0; iw < W - 1; ++iw) {
-                const int64_t off = shfl64(mine.off[iw], g + j);
-                cached[j][iw] = make_uint4(0u, 0u, 0u, 0u);
-                if (active && ((kinds >> (2 * iw)) & 3) == kTapCache)
-                    cached[j][iw] = *reinterpret_cast<const uint4 *>(a.cache + off + chan_off);
-            }
+        for (int iw = 0; iw < W; ++iw) {
+            const int kind = (kinds >> (2 * iw)) & 3;
+            // The token's own position (iw = W-1) comes from the cache only
+            // when its query start lies after it (inconsistent metadata); it
+            // is read like any other cached tap.
+            tap[iw] = kind == kTapX      ? xs[(u + iw) * nthreads]
+                      : kind == kTapCache ? *reinterpret_cast<const uint4 *>(a.cache + plan.off[u][iw] + chan_off)
+                                          : make_uint4(0u, 0u, 0u, 0u);
         }
+        if (ins >= 0) *reinterpret_cast<uint4 *>(a.cache + ins + chan_off) = xr;
+        float acc[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-        for (int j = 0; j < kGroup; ++j) {
-            const int u = g + j;
-            if (u >= n) break;  // warp-uniform
-            const int kinds = __shfl_sync(kFullMask, mine.kinds, u);
-            const int64_t ins = shfl64(mine.ins, u);
-            const int64_t off_last = shfl64(mine.off[W - 1], u);
-            const uint4 xr = xs[(u + W - 1) * 32];
-            if (active && ins >= 0) *reinterpret_cast<uint4 *>(a.cache + ins + chan_off) = xr;
-            float acc[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+        for (int iw = 0; iw < W; ++iw)
 #pragma unroll
-            for (int iw = 0; iw < W; ++iw) {
-                const int kind = (kinds >> (2 * iw)) & 3;
-                if (kind == kTapZero) continue;
-                uint4 tap = make_uint4(0u, 0u, 0u, 0u);
-                if (kind == kTapX) tap = xs[(u + iw) * 32];
-                else if (iw < W - 1) tap = cached[j][iw < W - 1 ? iw : 0];
-                // The token's own position comes from the cache only when its
-                // query start lies after it (inconsistent metadata).
-                else if (active) tap = *reinterpret_cast<const uint4 *>(a.cache + off_last + chan_off);
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    fma_bf16x2(acc[2 * q], acc[2 * q + 1], word_of(tap, q), word_of(wpk[iw], q));
-            }
-            const uint4 o = finish_row<SILU, RESID>(acc, xr);
-            if (active) __stcs(reinterpret_cast<uint4 *>(a.out + (t0 + u) * a.os_t + c0), o);
-        }
+            for (int q = 0; q < 4; ++q)
+                fma_bf16x2(acc[2 * q], acc[2 * q + 1], word_of(tap[iw], q), word_of(wpk[iw], q));
+        __stcs(reinterpret_cast<uint4 *>(op), finish_row<SILU, RESID>(acc, xr));
+        op += a.os_t;
     }
 }
 
 using ScalarFn = void (*)(PagedArgs);
-using VecFn = void (*)(PagedLaunch);
-
-template <int W>
-VecFn pick_vec_w(bool silu, bool resid) {
-    if (silu) return resid ? paged_vec_kernel<W, true, true> : paged_vec_kernel<W, true, false>;
-    return resid ? paged_vec_kernel<W, false, true> : paged_vec_kernel<W, false, false>;
-}
 
 template <int W>
 ScalarFn pick_scalar_w(bool silu, bool resid) {
     if (silu) return resid ? paged_scalar_kernel<W, true, true> : paged_scalar_kernel<W, true, false>;
     return resid ? paged_scalar_kernel<W, false, true> : paged_scalar_kernel<W, false, false>;
-}
-
-VecFn pick_vec(int width, bool silu, bool resid) {
-    switch (width) {
-        case 2: return pick_vec_w<2>(silu, resid);
-        case 3: return pick_vec_w<3>(silu, resid);
-        case 4: return pick_vec_w<4>(silu, resid);
-        case 5: return pick_vec_w<5>(silu, resid);
-    }
-    return nullptr;
 }
 
 ScalarFn pick_scalar(int width, bool silu, bool resid) {
@@ -487,16 +472,6 @@ ScalarFn pick_scalar(int width, bool silu, bool resid) {
         case 5: return pick_scalar_w<5>(silu, resid);
     }
     return nullptr;
-}
-
-int vec_smem(int width) {
-    switch (width) {
-        case 2: return vec_smem_bytes<2>();
-        case 3: return vec_smem_bytes<3>();
-        case 4: return vec_smem_bytes<4>();
-        case 5: return vec_smem_bytes<5>();
-    }
-    return 0;
 }
 
 constexpr int kMetaThreads = 256;
@@ -635,6 +610,32 @@ bool vec_ok(const PagedShared &p, const ccv_paged_stream &st) {
 }
 
 // Launch the given streams (all vector-capable) as one grid, blockIdx.z = stream.
+// The row kernel for width W with its shared-memory limit raised, once per
+// device, to what its largest block needs.
+template <int W, bool SILU, bool RESID>
+int launch_row_w(const PagedLaunch &pl, dim3 grid, int threads, ccv_stream_t stream) {
+    constexpr size_t kMaxBytes = sizeof(uint4) * kRowMaxThreads * row_slots<W>();
+    int dev = 0;
+    current_device_sms(&dev);
+    cudaError_t e;
+    if (resident_blocks<paged_row_kernel<W, SILU, RESID>>(kRowMaxThreads, kMaxBytes, dev, &e) == 0)
+        return static_cast<int>(e);
+    const size_t bytes = sizeof(uint4) * static_cast<size_t>(threads) * row_slots<W>();
+    return launch_pdl(paged_row_kernel<W, SILU, RESID>, grid, dim3(threads), bytes, stream, pl);
+}
+
+template <int W>
+int launch_row(const PagedLaunch &pl, dim3 grid, int threads, bool silu, bool resid,
+               ccv_stream_t stream) {
+    if (silu) return resid ? launch_row_w<W, true, true>(pl, grid, threads, stream)
+                           : launch_row_w<W, true, false>(pl, grid, threads, stream);
+    return resid ? launch_row_w<W, false, true>(pl, grid, threads, stream)
+                 : launch_row_w<W, false, false>(pl, grid, threads, stream);
+}
+
+// Launch the given streams (all vector-capable) as one grid, blockIdx.z =
+// stream: blocks of kRowRun tokens by up to kRowMaxThreads * 8 channels
+// (fewer threads when the widest stream is narrower).
 int launch_vec(const PagedShared &p, const ccv_paged_stream *streams, int n, ccv_stream_t stream) {
     PagedLaunch pl;
     pl.a = shared_args(p);
@@ -642,12 +643,20 @@ int launch_vec(const PagedShared &p, const ccv_paged_stream *streams, int n, ccv
     for (int i = 0; i < kMaxStreams; ++i) pl.s[i] = stream_fields(p, streams[i < n ? i : 0]);
     for (int i = 0; i < n; ++i) max_c = pl.s[i].C > max_c ? pl.s[i].C : max_c;
     apply_stream(pl.a, pl.s[0]);
-    const dim3 grid(static_cast<unsigned>((p.T + kVecBlockTokens - 1) / kVecBlockTokens),
-                    static_cast<unsigned>((max_c + kVecChannels - 1) / kVecChannels),
+    const int vecs = (max_c + 7) / 8;
+    const int threads = vecs >= kRowMaxThreads ? kRowMaxThreads : (vecs + 31) / 32 * 32;
+    const dim3 grid(static_cast<unsigned>((p.T + kRowRun - 1) / kRowRun),
+                    static_cast<unsigned>((max_c + threads * 8 - 1) / (threads * 8)),
                     static_cast<unsigned>(n));
     if (grid.y > 65535u) return CCV_ERR_SIZE;
-    return launch_pdl(pick_vec(p.width, p.silu != 0, p.residual != 0), grid, dim3(kThreads),
-                      vec_smem(p.width), stream, pl);
+    const bool silu = p.silu != 0, resid = p.residual != 0;
+    switch (p.width) {
+        case 2: return launch_row<2>(pl, grid, threads, silu, resid, stream);
+        case 3: return launch_row<3>(pl, grid, threads, silu, resid, stream);
+        case 4: return launch_row<4>(pl, grid, threads, silu, resid, stream);
+        case 5: return launch_row<5>(pl, grid, threads, silu, resid, stream);
+    }
+    return CCV_ERR_WIDTH;
 }
 
 int launch_scalar(const PagedShared &p, const ccv_paged_stream &st, ccv_stream_t stream) {

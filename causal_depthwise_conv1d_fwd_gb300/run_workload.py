@@ -8,7 +8,8 @@ Parts: prefill_tokens_dim, prefill_dim_tokens (4 x 4096 tokens, dim 8192),
 decode (256 x 8192; prefill parts take --width), paged (H16 x ws128, 32 requests; metadata + conv),
 spec (speculative verify, 64 rows x 4 drafts, dim 8192), atrex (one
 channel-first sequence of --tokens x --dim, the atrex-bench #003 shapes),
-paged_streams (a layer's four conv streams on one paged cache, one launch).
+paged_streams (a layer's four conv streams on one paged cache, one launch),
+varlen (8 sequences of 1..512 tokens, dim 4096, channel-last).
 The process exits 0 after a device synchronize; it times nothing.
 """
 from __future__ import annotations
@@ -21,7 +22,7 @@ from . import api
 from . import workloads as wl
 
 PARTS = ("prefill_tokens_dim", "prefill_dim_tokens", "decode", "paged", "spec", "atrex",
-         "paged_streams")
+         "paged_streams", "varlen")
 
 
 def _dev(kwargs, dev):
@@ -72,6 +73,12 @@ def make_launch(part: str, dev, tokens: int = 1024, dim: int = 4096, width: int 
         return lambda: launch()
     if part == "atrex":
         d = _dev(wl.config_atrex(tokens, dim).kwargs(), dev)
+        out = torch.empty_strided(d["x"].shape, d["x"].stride(), dtype=torch.bfloat16,
+                                  device=dev)
+        launch = api.prepare_ccv_fwd(**d, out=out)
+        return lambda: launch()
+    if part == "varlen":
+        d = _dev(wl.config_varlen().kwargs(), dev)
         out = torch.empty_strided(d["x"].shape, d["x"].stride(), dtype=torch.bfloat16,
                                   device=dev)
         launch = api.prepare_ccv_fwd(**d, out=out)

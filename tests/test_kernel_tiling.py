@@ -19,6 +19,15 @@ checks that:
   consumed once, after it was issued;
 - the segments cover the chunk and fit the chunk's segment budget;
 - every segment starts on the 256-byte boundary the alignment promises.
+
+Short problems: fwd_cl_short_kernel and fwd_cf_short_kernel find their chunk
+with a search whose final round also fetches every candidate's end, state
+line and flag; a replay checks that every chunk gets exactly one slot.  The
+channel-first short kernel covers a chunk with a window of kShortSegs
+256-token segments from the 16-byte boundary at or before its first token,
+plus the vector before the window: a replay checks that the window and that
+vector hold every input the chunk's outputs need, that each output token is
+stored exactly once and that whole-vector stores stay inside the chunk.
 """
 from __future__ import annotations
 
@@ -36,7 +45,7 @@ def _constants():
     common = open(os.path.join(CSRC, "ccv_common.cuh")).read()
     env = {"kMaxWidth": int(re.search(r"constexpr int kMaxWidth = (\d+);", common).group(1))}
     for name in ("kCfaSegs", "kCfaAlign", "kCfaSlots", "kCfaChunk", "kCaThreads", "kCaWarps",
-                 "kCaRun", "kCaChunk"):
+                 "kCaRun", "kCaChunk", "kShortRun", "kShortSegs", "kShortCfChunk"):
         expr = re.search(rf"constexpr int {name} = ([^;]+);", src).group(1)
         env[name] = int(eval(expr, {"__builtins__": {}}, dict(env)))
     return env
@@ -196,3 +205,96 @@ def test_chunk_slots_cover_every_chunk_once(C):
                 found[r] = slot
         want = {(i, k) for i, n in enumerate(lens) for k in range((n + C - 1) // C)}
         assert set(found) == want
+
+
+def locate_short(qsl, total, C, slot):
+    """The short kernels' search: 32-wide narrowing rounds while more than 32
+    candidates remain, then one round over at most 32 candidates that picks
+    the last with floor(qsl[i] / C) + i <= slot."""
+    lo, n = 0, len(qsl) - 1
+    while n > 32:
+        stride = (n + 31) >> 5
+        mask = 0
+        for lane in range(32):
+            off = lane * stride
+            if off < n and qsl[lo + off] // C + lo + off <= slot:
+                mask |= 1 << lane
+        if mask == 0:
+            return None
+        top = mask.bit_length() - 1
+        lo += top * stride
+        n = min(stride, n - top * stride)
+    mask = 0
+    for lane in range(32):
+        if lane < n and qsl[lo + lane] // C + lo + lane <= slot:
+            mask |= 1 << lane
+    if mask == 0:
+        return None
+    seq = lo + mask.bit_length() - 1
+    start, end = qsl[seq], qsl[seq + 1]
+    if start < 0 or end < start or end > total:
+        return None
+    k = slot - (start // C + seq)
+    if k < 0 or k * C >= end - start:
+        return None
+    return seq, k
+
+
+@pytest.mark.parametrize("C", ["kShortRun", "kShortCfChunk"])
+def test_short_chunk_slots_cover_every_chunk_once(C):
+    import random
+
+    C = K[C]
+    rng = random.Random(11)
+    for trial in range(60):
+        batch = rng.choice([1, 2, 3, 31, 32, 33, 100, 1025])
+        lens = [rng.choice([0, 1, 2, C - 1, C, C + 1, rng.randrange(0, 3 * C)])
+                for _ in range(batch)]
+        qsl = [0]
+        for n in lens:
+            qsl.append(qsl[-1] + n)
+        total = qsl[-1] + rng.choice([0, 0, 5])
+        found = {}
+        for slot in range(total // C + batch):
+            r = locate_short(qsl, total, C, slot)
+            if r is not None:
+                assert r not in found, f"chunk {r} found by slots {found[r]} and {slot}"
+                found[r] = slot
+        want = {(i, k) for i, n in enumerate(lens) for k in range((n + C - 1) // C)}
+        assert set(found) == want
+
+
+@pytest.mark.parametrize("W", [2, 3, 4, 5])
+def test_short_channel_first_window(W):
+    """For every row phase and a set of chunk positions, the inputs the
+    chunk's outputs read (tokens cbeg-(W-1) .. cend-1) lie in the window or
+    the vector before it, and every output token is stored once, whole-vector
+    stores only inside [cbeg, cend).  (Loads take a whole vector only when
+    all 8 tokens lie inside the row, by the kernel's own test.)"""
+    CH, SEGS = K["kShortCfChunk"], K["kShortSegs"]
+    for total in (1, 7, 8, 300, CH - 1, CH, CH + 1, 3 * CH + 5):
+        starts = sorted({0, 1, 3, 8, max(0, total - CH - 2), max(0, total - 1)})
+        for start in starts:
+            if start >= total:
+                continue
+            length = total - start
+            for chunk in range((length + CH - 1) // CH):
+                cbeg = start + chunk * CH
+                cend = start + min(length, (chunk + 1) * CH)
+                for phase in range(8):
+                    a0 = cbeg - ((phase + cbeg) & 7)
+                    assert (phase + a0) % 8 == 0 and cbeg - 8 < a0 <= cbeg
+                    held = set(range(a0 - 8, a0 + 256 * SEGS))
+                    need = set(range(cbeg - (W - 1), cend))
+                    assert need <= held, (total, start, chunk, phase)
+                    stored = []
+                    for sg in range(SEGS):
+                        for lane in range(32):
+                            t0 = a0 + sg * 256 + lane * 8
+                            if t0 + 8 <= cbeg or t0 >= cend:
+                                continue
+                            if t0 >= cbeg and t0 + 8 <= cend:
+                                stored += range(t0, t0 + 8)
+                            else:
+                                stored += [t for t in range(t0, t0 + 8) if cbeg <= t < cend]
+                    assert sorted(stored) == list(range(cbeg, cend)), (total, start, chunk, phase)

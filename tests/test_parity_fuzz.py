@@ -23,7 +23,10 @@ DEV = torch.device("cuda", 0)
 
 
 @pytest.mark.parametrize("seed", range(120))
-def test_fwd_random(seed):
+def test_fwd_random(seed, monkeypatch):
+    # even seeds through the streaming prefill kernels, odd ones through the
+    # short-problem kernels
+    monkeypatch.setenv("CCV_PREFILL_PATH", "stream" if seed % 2 == 0 else "short")
     r = random.Random(7000 + seed)
     width = r.randint(2, 5)
     batch = r.randint(1, 6)

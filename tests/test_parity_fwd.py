@@ -1,4 +1,6 @@
-"""GPU parity of ccv_fwd (varlen prefill) against the CPU oracle.
+"""GPU parity of ccv_fwd (varlen prefill) against the CPU oracle, through
+both kernel families (forced by CCV_PREFILL_PATH) and through the automatic
+choice on both sides of its size threshold.
 
 Outputs within 1e-2*|ref| + 2e-5, conv_state bit-exact, untouched regions
 (pad sequences, zero-length sequences, wider state columns, guard bands)
@@ -18,6 +20,15 @@ from parity_util import assert_bits, assert_close, sentinel_like, to_device
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda", 0)
+
+
+@pytest.fixture(params=["short", "stream"], autouse=True)
+def prefill_path(request, monkeypatch):
+    """Every case runs through both prefill kernel families: the short-problem
+    kernels (a warp per short chunk, inputs straight into registers) and the
+    streaming ones (block chunks through shared-memory rings)."""
+    monkeypatch.setenv("CCV_PREFILL_PATH", request.param)
+    return request.param
 
 
 def run_both(case, out_cpu=None, out_dev=None, err=False):
@@ -348,3 +359,37 @@ def test_strided_bias_is_rejected():
         ccv.ccv_update(**dc)
     with pytest.raises(ValueError, match="contiguous"):
         ccv.ccv_update_spec(**dc)
+
+
+def _kernel_names(fn):
+    """Names of the CUDA kernels `fn` launches, or None without a profiler."""
+    try:
+        from torch.profiler import ProfilerActivity, profile
+        with profile(activities=[ProfilerActivity.CUDA]) as prof:
+            fn()
+            torch.cuda.synchronize()
+        return [e.name for e in prof.events() if e.device_type.name == "CUDA"]
+    except Exception:  # no CUPTI in this build
+        return None
+
+
+@pytest.mark.parametrize("layout", ["tokens_dim", "dim_tokens"])
+@pytest.mark.parametrize("tokens", [2048, 2049])
+def test_automatic_choice_at_its_threshold(prefill_path, monkeypatch, layout, tokens):
+    """Without CCV_PREFILL_PATH the size decides: total_tokens x dim up to 2^23
+    elements takes the short kernels, more takes the streaming ones.  At dim
+    4096, 2048 tokens is the last short problem and 2049 the first streaming
+    one; both match the oracle."""
+    if prefill_path == "stream":
+        pytest.skip("the automatic choice is the same for both fixture values")
+    monkeypatch.delenv("CCV_PREFILL_PATH")
+    case = wl.varlen_prefill(1700 + tokens, [tokens - 700, 3, 697], 4096, 4, num_cache_lines=4,
+                             layout=layout, pad_positions=(1,), has_init="bernoulli")
+    ref_out, ref_states, out, states, _ = run_both(case)
+    assert_close(out, ref_out, f"threshold {tokens} out")
+    assert_bits(states, ref_states, f"threshold {tokens} states")
+    d = to_device(case.kwargs(), DEV)
+    names = _kernel_names(lambda: ccv.ccv_fwd(**d))
+    if names is not None:
+        want = "short" if tokens * 4096 <= (1 << 23) else "async"
+        assert any(want in n for n in names), names
