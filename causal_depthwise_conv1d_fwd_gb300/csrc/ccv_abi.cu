@@ -21,4 +21,5 @@ extern "C" const char *ccv_status_string(int status) {
 }
 
 // 1.1.0: ccv_update_spec and paged_sconv_fwd_streams added.
-extern "C" int ccv_version(void) { return 1 * 10000 + 1 * 100 + 0; }
+// 1.2.0: programmatic dependent launches; short-problem prefill kernels.
+extern "C" int ccv_version(void) { return 1 * 10000 + 2 * 100 + 0; }

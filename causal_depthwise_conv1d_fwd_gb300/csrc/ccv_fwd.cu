@@ -959,7 +959,7 @@ __global__ void __launch_bounds__(kCfaThreads, 4) fwd_cf_async_kernel(const FwdA
 constexpr int kShortThreads = 128;
 constexpr int kShortWarps = kShortThreads / 32;
 constexpr int kShortRun = 8;  // channel-last: tokens per warp (one run)
-constexpr int kShortSegs = 2;  // channel-first: 256-token segments per warp
+constexpr int kShortSegs = 5;  // channel-first: 256-token segments per warp
 // channel-first chunk: a window of kShortSegs * 256 tokens that starts on the
 // 16-byte boundary at or before the chunk's first token covers it
 constexpr int kShortCfChunk = kShortSegs * 256 - 8;
@@ -1020,9 +1020,17 @@ __device__ __forceinline__ bool locate_short(const FwdArgs &a, int chunk_tokens,
 }
 
 // Channel-last: warp = (run of kShortRun tokens, 256-channel tile), lane =
-// 8 channels; global warp g = slot * tiles + tile.
+// 8 channels; global warp g = slot * tiles + tile.  Every input row of the
+// run goes to shared memory by asynchronous copies (no registers held while
+// in flight, so a full grid fits the machine in one wave): slot rows
+// [0, W-1) the inputs before the run, [W-1, W-1+n) the run, and for a
+// sequence's first run [kShortRun+W-1, kShortRun+2W-2) the rows its new
+// state takes from x.
+constexpr int kShortClSlots = kShortRun + 2 * (kMaxWidth - 1);
+
 template <int W, bool SILU>
-__global__ void __launch_bounds__(kShortThreads) fwd_cl_short_kernel(const FwdArgs a, int nslots) {
+__global__ void __launch_bounds__(kShortThreads, 7) fwd_cl_short_kernel(const FwdArgs a, int nslots) {
+    __shared__ __align__(16) uint4 s_rows[kShortClSlots * kShortThreads];
     release_next_grid();
     wait_prior_grid();
     const int lane = threadIdx.x & 31;
@@ -1039,27 +1047,46 @@ __global__ void __launch_bounds__(kShortThreads) fwd_cl_short_kernel(const FwdAr
 
     const int64_t xs = a.xs_t;
     const uint16_t *xc = a.x + c0;
+    uint4 *rows = s_rows + threadIdx.x;  // slot m at rows[m * kShortThreads]
     const int r0 = sc.start + sc.chunk * kShortRun;
     const int n = min(kShortRun, sc.len - sc.chunk * kShortRun);
     const bool first = sc.chunk == 0;
-    // Every load of the chunk goes out at once: its rows, the W-1 inputs
-    // before it (x rows, or the state columns for a sequence's first run)
-    // and, for the first run, the rows the new state takes from x.
-    uint4 v[kShortRun];
+    const bool write_state = first && a.st != nullptr;
 #pragma unroll
     for (int m = 0; m < kShortRun; ++m)
-        v[m] = m < n ? __ldg(reinterpret_cast<const uint4 *>(xc + (r0 + m) * xs)) : make_uint4(0u, 0u, 0u, 0u);
+        if (m < n) cp_async16(rows + (W - 1 + m) * kShortThreads, xc + (r0 + m) * xs);
+    if (!first) {
+#pragma unroll
+        for (int j = 0; j < W - 1; ++j)
+            cp_async16(rows + j * kShortThreads, xc + (r0 - (W - 1) + j) * xs);
+    }
+    if (write_state) {
+        // New state = last W-1 entries of prior ++ x[sequence]; the entries
+        // that come from x are copied in here.
+#pragma unroll
+        for (int j = 0; j < W - 1; ++j) {
+            const int idx = sc.len + j;
+            if (idx >= W - 1)
+                cp_async16(rows + (kShortRun + W - 1 + j) * kShortThreads,
+                           xc + (sc.start + idx - (W - 1)) * xs);
+        }
+    }
+    cp_async_commit();
     uint4 ring[W - 1];
 #pragma unroll
     for (int j = 0; j < W - 1; ++j) {
         ring[j] = make_uint4(0u, 0u, 0u, 0u);
-        if (!first) ring[j] = *reinterpret_cast<const uint4 *>(xc + (r0 - (W - 1) + j) * xs);
-        else if (sc.init) ring[j] = load8_state(a, sc.line, c0, j);
+        if (first && sc.init) ring[j] = load8_state(a, sc.line, c0, j);
     }
+    uint4 wpk[W];
+    const bool w_vec = a.ws_k == 1 && a.ws_d == W && (reinterpret_cast<uintptr_t>(a.w) & 15u) == 0;
+    load_weights8<W>(a.w, a.ws_d, a.ws_k, c0, a.dim, w_vec, wpk);
+    float bs[8];
+    load_bias8(a.bias, c0, a.dim, (reinterpret_cast<uintptr_t>(a.bias) & 15u) == 0, bs);
+    cp_async_wait<0>();
+
     uint4 nw[W - 1];
-    const bool write_state = first && a.st != nullptr;
     if (write_state) {
-        // New state = last W-1 entries of prior ++ x[sequence].
 #pragma unroll
         for (int j = 0; j < W - 1; ++j) {
             const int idx = sc.len + j;
@@ -1068,25 +1095,24 @@ __global__ void __launch_bounds__(kShortThreads) fwd_cl_short_kernel(const FwdAr
                 for (int q = 0; q < W - 1; ++q)
                     if (q == idx) nw[j] = ring[q];
             } else {
-                nw[j] = *reinterpret_cast<const uint4 *>(xc + (sc.start + idx - (W - 1)) * xs);
+                nw[j] = rows[(kShortRun + W - 1 + j) * kShortThreads];
             }
         }
     }
-    uint4 wpk[W];
-    const bool w_vec = a.ws_k == 1 && a.ws_d == W && (reinterpret_cast<uintptr_t>(a.w) & 15u) == 0;
-    load_weights8<W>(a.w, a.ws_d, a.ws_k, c0, a.dim, w_vec, wpk);
-    float bs[8];
-    load_bias8(a.bias, c0, a.dim, (reinterpret_cast<uintptr_t>(a.bias) & 15u) == 0, bs);
-
+    if (!first) {
+#pragma unroll
+        for (int j = 0; j < W - 1; ++j) ring[j] = rows[j * kShortThreads];
+    }
     uint16_t *dst = a.out + c0 + static_cast<int64_t>(r0) * a.os_t;
 #pragma unroll
     for (int m = 0; m < kShortRun; ++m) {
         if (m >= n) break;
-        __stcs(reinterpret_cast<uint4 *>(dst), ca_row<W, SILU>(wpk, bs, ring, v[m]));
+        const uint4 v = rows[(W - 1 + m) * kShortThreads];
+        __stcs(reinterpret_cast<uint4 *>(dst), ca_row<W, SILU>(wpk, bs, ring, v));
         dst += a.os_t;
 #pragma unroll
         for (int k = 0; k < W - 2; ++k) ring[k] = ring[k + 1];
-        ring[W - 2] = v[m];
+        ring[W - 2] = v;
     }
     if (write_state) {
 #pragma unroll
@@ -1094,40 +1120,41 @@ __global__ void __launch_bounds__(kShortThreads) fwd_cl_short_kernel(const FwdAr
     }
 }
 
-// The 8 logical inputs at tokens t0..t0+7 of one channel-first row, from
-// `raw` (those tokens as loaded where they lie inside [0, total), else 0):
-// x inside [lo, cend), the prior (packed, oldest first) just before a
-// sequence's first chunk, 0 elsewhere.
+// The 8 inputs at tokens t0..t0+7 of a sequence's first chunk as its
+// outputs see them: the prior (packed, oldest first) at the W-1 tokens
+// before cbeg, `raw` (x as loaded) elsewhere.  Tokens further back feed no
+// output of the chunk, nor do tokens at or past its end, so they keep
+// whatever `raw` holds.  Only the one or two vectors that reach before cbeg
+// get here, out of line.
 template <int W>
-__device__ __forceinline__ uint4 short_mask(uint4 raw, int t0, int lo, int cbeg, int cend, bool chunk0,
-                                            uint32_t prior01, uint32_t prior23) {
-    if (t0 >= lo && t0 + 8 <= cend) return raw;
+__device__ __noinline__ uint4 short_prior_edge(uint4 raw, int t0, int cbeg, uint32_t prior01,
+                                               uint32_t prior23) {
     uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        uint32_t pair = 0;
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-            const int t = t0 + 2 * q + e;
-            uint32_t val = 0;
-            if (t >= lo && t < cend) {
-                val = e ? (w[q] >> 16) : (w[q] & 0xffffu);
-            } else if (chunk0 && t >= cbeg - (W - 1) && t < cbeg) {
-                const int i = t - cbeg + (W - 1);  // prior column
+            const int i = t0 + 2 * q + e - cbeg + (W - 1);  // prior column, if in [0, W-1)
+            if (i >= 0 && i < W - 1) {
                 const uint32_t src = i < 2 ? prior01 : prior23;
-                val = (i & 1) ? (src >> 16) : (src & 0xffffu);
+                const uint32_t val = (i & 1) ? (src >> 16) : (src & 0xffffu);
+                w[q] = e ? ((w[q] & 0x0000ffffu) | (val << 16)) : ((w[q] & 0xffff0000u) | val);
             }
-            pair |= val << (16 * e);
         }
-        w[q] = pair;
     }
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// Tokens t0..t0+7 of row xc as loaded: one 16-byte load when all lie inside
-// [0, total) (t0 is on a 16-byte boundary), else element by element.
-__device__ __forceinline__ uint4 short_load(const uint16_t *xc, int t0, int total) {
-    if (t0 >= 0 && t0 + 8 <= total) return __ldg(reinterpret_cast<const uint4 *>(xc + t0));
+template <int W>
+__device__ __forceinline__ uint4 short_prior(uint4 raw, int t0, int cbeg, uint32_t prior01,
+                                             uint32_t prior23) {
+    if (t0 >= cbeg || t0 + 8 <= cbeg - (W - 1)) return raw;
+    return short_prior_edge<W>(raw, t0, cbeg, prior01, prior23);
+}
+
+// Tokens t0..t0+7 of a row that starts or ends inside them, element by
+// element (0 outside [0, total)); out of line, like the edge masking.
+__device__ __noinline__ uint4 short_load_edge(const uint16_t *xc, int t0, int total) {
     uint32_t w[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -1137,6 +1164,13 @@ __device__ __forceinline__ uint4 short_load(const uint16_t *xc, int t0, int tota
         w[q] = lo | (hi << 16);
     }
     return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Tokens t0..t0+7 of row xc as loaded: one 16-byte load when all lie inside
+// [0, total) (t0 is on a 16-byte boundary), else element by element.
+__device__ __forceinline__ uint4 short_load(const uint16_t *xc, int t0, int total) {
+    if (t0 >= 0 && t0 + 8 <= total) return __ldg(reinterpret_cast<const uint4 *>(xc + t0));
+    return short_load_edge(xc, t0, total);
 }
 
 // Channel-first: warp = (chunk of kShortCfChunk tokens, channel row), as
@@ -1160,14 +1194,16 @@ __global__ void __launch_bounds__(kShortThreads) fwd_cf_short_kernel(const FwdAr
     const int cbeg = sc.start + sc.chunk * kShortCfChunk;
     const int cend = sc.start + min(sc.len, (sc.chunk + 1) * kShortCfChunk);
     const bool chunk0 = sc.chunk == 0;
-    const int lo = chunk0 ? cbeg : cbeg - (W - 1);
     const int phase = static_cast<int>((reinterpret_cast<uintptr_t>(xc) >> 1) & 7u);
     const int a0 = cbeg - ((phase + cbeg) & 7);  // on a 16-byte boundary, a0 > cbeg - 8
     // Every load goes out at once: the window's vectors, the vector before
     // it (lane 0), the state columns and the inputs the new state takes.
     uint4 raw[kShortSegs];
 #pragma unroll
-    for (int sg = 0; sg < kShortSegs; ++sg) raw[sg] = short_load(xc, a0 + sg * 256 + lane * 8, a.total);
+    for (int sg = 0; sg < kShortSegs; ++sg) {
+        raw[sg] = make_uint4(0u, 0u, 0u, 0u);
+        if (a0 + sg * 256 < cend) raw[sg] = short_load(xc, a0 + sg * 256 + lane * 8, a.total);  // warp-uniform
+    }
     uint4 raw_before = make_uint4(0u, 0u, 0u, 0u);
     if (lane == 0) raw_before = short_load(xc, a0 - 8, a.total);
     uint32_t p[4] = {0, 0, 0, 0};
@@ -1186,13 +1222,18 @@ __global__ void __launch_bounds__(kShortThreads) fwd_cf_short_kernel(const FwdAr
     const float bs = a.bias ? bf16_bits(__ldg(a.bias + c)) : 0.0f;
 
     const uint32_t prior01 = p[0] | (p[1] << 16), prior23 = p[2] | (p[3] << 16);
-    const uint4 before = short_mask<W>(raw_before, a0 - 8, lo, cbeg, cend, chunk0, prior01, prior23);
-    uint32_t prev_z = before.z, prev_w = before.w;  // tokens a0-4 .. a0-1 (lane 0)
+    uint32_t prev_z = 0, prev_w = 0;  // lane 0: tokens a0-4 .. a0-1
+    if (lane == 0) {
+        const uint4 before = chunk0 ? short_prior<W>(raw_before, a0 - 8, cbeg, prior01, prior23) : raw_before;
+        prev_z = before.z;
+        prev_w = before.w;
+    }
     uint16_t *const oc = a.out + c * a.os_d;
 #pragma unroll
     for (int sg = 0; sg < kShortSegs; ++sg) {
+        if (a0 + sg * 256 >= cend) break;  // warp-uniform: the chunk ends before this segment
         const int t0 = a0 + sg * 256 + lane * 8;
-        const uint4 v = short_mask<W>(raw[sg], t0, lo, cbeg, cend, chunk0, prior01, prior23);
+        const uint4 v = chunk0 && sg == 0 ? short_prior<W>(raw[sg], t0, cbeg, prior01, prior23) : raw[sg];
         const uint32_t up_z = __shfl_up_sync(kFullMask, v.z, 1);
         const uint32_t up_w = __shfl_up_sync(kFullMask, v.w, 1);
         const uint32_t pv_z = __shfl_sync(kFullMask, prev_z, sg == 0 ? 0 : 31);

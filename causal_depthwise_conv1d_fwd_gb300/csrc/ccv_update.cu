@@ -257,14 +257,11 @@ __global__ void __launch_bounds__(kThreads, VEC == 8 ? 7 : 1) update_kernel(cons
     const bool active = c0 < a.dim;
 
     if constexpr (VEC == 8) {
-        uint4 wpk[W];
-        float bs[8];
-        if (active) {
-            load_weights8<W>(a.w, a.ws_d, a.ws_k, c0, a.dim, a.w_vec, wpk);
-            load_bias8(a.bias, c0, a.dim, a.b_vec, bs);
-        }
-        // The rows' inputs do not depend on their state lines either: they go
-        // out with the index loads, so only the state windows wait for them.
+        // The state-line indices gate the only dependent loads, so they go
+        // out first; the rows' inputs, the weights and the bias do not depend
+        // on them and follow, so only the state windows wait for the lines.
+        int lines[kRows];
+        resolve_lines(a, rg, active, c0, lines);
         uint4 xv[kRows];
 #pragma unroll
         for (int r = 0; r < kRows; ++r) {
@@ -272,8 +269,12 @@ __global__ void __launch_bounds__(kThreads, VEC == 8 ? 7 : 1) update_kernel(cons
             xv[r] = make_uint4(0u, 0u, 0u, 0u);
             if (active && b < a.batch) xv[r] = gather<8>(a.x + b * a.xs_b + c0 * a.xs_d, a.xs_d, a.x_vec).v;
         }
-        int lines[kRows];
-        resolve_lines(a, rg, active, c0, lines);
+        uint4 wpk[W];
+        float bs[8];
+        if (active) {
+            load_weights8<W>(a.w, a.ws_d, a.ws_k, c0, a.dim, a.w_vec, wpk);
+            load_bias8(a.bias, c0, a.dim, a.b_vec, bs);
+        }
         uint4 win[kRows][W - 1];
 #pragma unroll
         for (int r = 0; r < kRows; ++r) {

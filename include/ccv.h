@@ -20,6 +20,11 @@
  *   argument error detected on the host (nothing is launched); a positive
  *   value is the cudaError_t of a failed launch.
  * - Size 0 work (no tokens, no rows) returns CCV_OK without launching.
+ * - Kernels are launched with programmatic stream serialization: a kernel's
+ *   blocks may be scheduled while the previous kernel on the stream is still
+ *   finishing, but each waits for that kernel to complete before it reads or
+ *   writes any memory, so stream order holds exactly as for plain launches
+ *   (and under CUDA-graph capture).
  * - `err_count` (nullable) is a device int the kernels atomically increment
  *   when they skip data-dependent invalid indices (a query_start_loc that
  *   decreases or leaves [0, total_tokens], a state line outside
@@ -89,6 +94,10 @@ int ccv_version(void);
  *               Requires conv_states.
  * A zero-length sequence writes nothing.  silu != 0 applies v/(1+exp(-v)).
  * Two non-pad sequences that share a state line race (undefined result).
+ * Problems of up to 2^23 elements (total_tokens * dim) run on kernels built
+ * for latency, larger ones on streaming kernels; both compute the same
+ * results.  The environment variable CCV_PREFILL_PATH=short or =stream,
+ * read at each call, forces one family (for testing and tuning).
  */
 int ccv_fwd(const void *x, int64_t x_stride_dim, int64_t x_stride_tok,
             void *out, int64_t out_stride_dim, int64_t out_stride_tok,

@@ -47,7 +47,7 @@ def test_status_strings(lib):
         s = _lib.status_string(code)
         assert s and "unknown" not in s
     assert "unknown" in _lib.status_string(-1000)
-    assert lib.ccv_version() == 10100
+    assert lib.ccv_version() == 10200
 
 
 def fwd(lib, **over):
