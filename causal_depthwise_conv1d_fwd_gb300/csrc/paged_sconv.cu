@@ -103,6 +103,8 @@ __device__ __forceinline__ void split_pos(const PagedArgs &a, int64_t p, int64_t
 constexpr int kTapZero = 0;    // PAD row or a position before 0: contributes nothing
 constexpr int kTapX = 1;       // in this forward: x row (t - (W-1) + iw)
 constexpr int kTapCache = 2;   // before this forward: cache entry at TokenPlan::off[iw]
+// A PAD row's kinds: every tap field zero, plus a flag bit above them.
+constexpr int kPadRow = 1 << 30;
 
 // What every channel of a token needs: where each tap comes from, and where
 // the token's input goes (ins < 0: nowhere).  Offsets exclude the channel's
@@ -143,7 +145,10 @@ __device__ __forceinline__ TokenPlan<W> plan_token(const PagedArgs &a, int t, co
     for (int iw = 0; iw < W; ++iw) p.off[iw] = 0;
     const int64_t slot = m.slot, pos = m.pos;
     const int req = m.req, qs = m.qs;
-    if (slot < 0) return p;  // PAD row: every tap is zero, nothing is inserted
+    if (slot < 0) {  // PAD row: every tap is zero, nothing is inserted
+        p.kinds = kPadRow;
+        return p;
+    }
     int64_t blk, boff;
     split_pos(a, slot, blk, boff);
     if (blk < a.num_blocks) p.ins = blk * a.cs_blk + boff * a.cs_n;
@@ -246,23 +251,25 @@ __global__ void __launch_bounds__(kThreads) paged_scalar_kernel(const PagedArgs 
 }
 
 // Row kernel: a block covers a run of kRowRun tokens across up to
-// kRowMaxThreads * 8 channels -- every channel of a 2048-channel stream --
-// with a thread per 8 consecutive channels (one 16-byte vector, all in one
-// head because ws is a multiple of 8).  Each thread first streams its x
-// vectors of the run and of the W-1 rows before it into a private ring of
-// shared-memory slots with asynchronous copies (it reads back only its own
-// slots, so its own wait is the only synchronisation for them).  Meanwhile
-// the first warp resolves every token's plan once -- the four index loads,
-// then the block-table lookups of its pre-forward taps -- into shared
+// kRowMaxThreads * 8 channels, a thread per 8 consecutive channels (one
+// 16-byte vector, all in one head because ws is a multiple of 8).  The first
+// warp's token metadata and every thread's weights are requested first;
+// then each thread streams its x vectors of the run and of the W-1 rows
+// before it into a private ring of shared-memory slots with asynchronous
+// copies (it reads back only its own slots, so its own wait is the only
+// synchronisation for them).  The first warp resolves every token's plan
+// once -- tap sources through the block table, insert slot -- into shared
 // memory, and one barrier publishes it to the block.  When every token of
-// the run takes all W taps from x and has an insert slot (an interior
-// stretch of a prefill, the usual case) a straight loop keeps the taps in a
-// register ring of raw bf16 rows; otherwise each token follows its plan (x
-// rows from the ring, cache taps from global memory).  Taps are native bf16
-// x bf16 + fp32 FMAs on packed weights; the residual enters the same way
-// (x * 1 + act, one rounding).
+// the run takes all W taps from x and has an insert slot, or is a PAD row
+// (an interior stretch of a prefill, the usual case), a straight loop keeps
+// the taps in a register ring of raw bf16 rows; otherwise each token
+// follows its plan (x rows from the ring, cache taps from global memory).
+// Taps are native bf16 x bf16 + fp32 FMAs on packed weights; the residual
+// enters the same way (x * 1 + act, one rounding).  Blocks of 128 threads
+// (two per 2048-channel run) spread the runs more evenly over the SMs than
+// one 256-thread block per run (measured faster).
 constexpr int kRowRun = 8;           // tokens per block (at most 32: one planning lane each)
-constexpr int kRowMaxThreads = 256;  // 2048 channels per block
+constexpr int kRowMaxThreads = 128;  // 1024 channels per block
 constexpr int kStageGroup = 4;       // staged rows per asynchronous-copy group
 
 // One run's plans, written by the first warp and read by every thread.
@@ -327,7 +334,7 @@ __device__ __forceinline__ uint4 paged_row(const uint4 (&wpk)[W], const uint4 (&
 }
 
 template <int W, bool SILU, bool RESID>
-__global__ void __launch_bounds__(kRowMaxThreads, 4) paged_row_kernel(const PagedLaunch pl) {
+__global__ void __launch_bounds__(kRowMaxThreads, 8) paged_row_kernel(const PagedLaunch pl) {
     extern __shared__ uint4 stage[];  // [row_slots<W>()][blockDim.x]
     __shared__ RunPlan<W> plan;
     constexpr int R = row_slots<W>();
@@ -357,8 +364,16 @@ __global__ void __launch_bounds__(kRowMaxThreads, 4) paged_row_kernel(const Page
     const bool active = c0 < a.C;
     uint4 *xs = stage + tid;  // row m of the run's window at xs[m * nthreads]
 
-    // The x stream goes out first: rows t0-(W-1) .. t0+n-1, in commit groups
+    // The first warp's token metadata and every thread's weights go out
+    // first: the plan waits on the one and the block's barrier on the other
+    // (the weights are regrouped as they arrive), and queued behind the x
+    // streams of all blocks, which go out at once, they would wait for all
+    // of them.  Then the x stream: rows t0-(W-1) .. t0+n-1, in commit groups
     // of kStageGroup rows so the straight loop can start on the first ones.
+    TokenMeta meta{-1, 0, 0, 0};
+    if (tid < 32) meta = load_meta(a, t0 + tid, tid < n);  // lane u: token t0 + u
+    uint4 wpk[W];
+    load_weights8<W>(a.w, a.ws_c, a.ws_k, active ? c0 : 0, a.C, a.w_vec, wpk);
 #pragma unroll
     for (int m = 0; m < R; ++m) {
         const int row = t0 - (W - 1) + m;
@@ -366,18 +381,19 @@ __global__ void __launch_bounds__(kRowMaxThreads, 4) paged_row_kernel(const Page
         else xs[m * nthreads] = make_uint4(0u, 0u, 0u, 0u);
         if (m % kStageGroup == kStageGroup - 1 || m == R - 1) cp_async_commit();
     }
-    uint4 wpk[W];
-    load_weights8<W>(a.w, a.ws_c, a.ws_k, active ? c0 : 0, a.C, a.w_vec, wpk);
     if (tid < 32) {
         // Lane u plans token t0 + u; lanes past the run carry an empty plan.
-        const TokenPlan<W> p = plan_token<W>(a, t0 + tid, load_meta(a, t0 + tid, tid < n));
+        const TokenPlan<W> p = plan_token<W>(a, t0 + tid, meta);
         if (tid < kRowRun) {
             plan.kinds[tid] = p.kinds;
             plan.ins[tid] = p.ins;
 #pragma unroll
             for (int iw = 0; iw < W; ++iw) plan.off[tid][iw] = p.off[iw];
         }
-        const bool ax = __all_sync(kFullMask, tid >= n || (p.kinds == all_x_kinds<W>() && p.ins >= 0));
+        // The straight loop serves tokens whose taps all come from x and
+        // that have an insert slot, and PAD rows.
+        const bool ax = __all_sync(kFullMask, tid >= n || p.kinds == kPadRow ||
+                                                  (p.kinds == all_x_kinds<W>() && p.ins >= 0));
         if (tid == 0) plan.all_x = ax;
     }
     __syncthreads();
@@ -404,8 +420,16 @@ __global__ void __launch_bounds__(kRowMaxThreads, 4) paged_row_kernel(const Page
             const int need = (u + W - 1) / kStageGroup;
             if (u > 0 && need != (u + W - 2) / kStageGroup) cp_async_wait_upto(kGroups - 1 - need);
             const uint4 xr = xs[(u + W - 1) * nthreads];
-            *reinterpret_cast<uint4 *>(a.cache + plan.ins[u] + chan_off) = xr;
-            __stcs(reinterpret_cast<uint4 *>(op), paged_row<W, SILU, RESID>(wpk, ring, xr));
+            const int64_t ins = plan.ins[u];
+            if (ins >= 0) {  // block-uniform
+                *reinterpret_cast<uint4 *>(a.cache + ins + chan_off) = xr;
+                __stcs(reinterpret_cast<uint4 *>(op), paged_row<W, SILU, RESID>(wpk, ring, xr));
+            } else {
+                // A PAD row: every tap is zero, so the output is act(0) plus
+                // the residual, and nothing is inserted.
+                float zero[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+                __stcs(reinterpret_cast<uint4 *>(op), finish_row<SILU, RESID>(zero, xr));
+            }
             op += a.os_t;
 #pragma unroll
             for (int m = 0; m < W - 2; ++m) ring[m] = ring[m + 1];
