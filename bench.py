@@ -883,6 +883,54 @@ def host_link_peak(dev, nbytes=1 << 30, reps=5):
     return out
 
 
+def back_to_back_us(part, calls=50):
+    """us per call of `calls` launches of one part back to back (events
+    around the whole loop), so each launch may overlap the previous one's
+    tail.  Meaningful L2-cold only for parts whose data exceed L2."""
+    for _ in range(3):
+        part.fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    stream = torch.cuda.current_stream()
+    a.record(stream)
+    for _ in range(calls):
+        part.fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) * 1e3 / calls
+
+
+def launch_floor_us(dev, calls=100):
+    """The cost of any launch as the parts and the extras are timed: a
+    one-element torch kernel, us per call back to back (events around many
+    calls) and one at a time after an L2 flush (events around each call,
+    the flush outside them), mean of many calls."""
+    tiny = torch.zeros(1, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(10):
+        tiny.add_(1.0)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(calls):
+        tiny.add_(1.0)
+    b.record(stream)
+    torch.cuda.synchronize()
+    b2b = a.elapsed_time(b) * 1e3 / calls
+    flush = L2Flush(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(calls)]
+    for e0, e1 in evs:
+        flush()
+        e0.record(stream)
+        tiny.add_(1.0)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    single = sum(e0.elapsed_time(e1) * 1e3 for e0, e1 in evs) / calls
+    return {"back_to_back": round(b2b, 2), "single_after_flush": round(single, 2),
+            "kernel": "one-element torch add"}
+
+
 def run_ours(args):
     import causal_depthwise_conv1d_fwd_gb300 as ccv  # noqa: F401
     from causal_depthwise_conv1d_fwd_gb300 import _lib
@@ -930,6 +978,7 @@ def run_ours(args):
     # event between two launches also serialises them).
     parts_s = time_parts(parts, args.steps, stream)
     graph = graph_step_timing(parts, args.steps)
+    b2b = {p.name: back_to_back_us(p) for p in parts if p.name.startswith("prefill")}
 
     step_bytes = sum(p.nbytes for p in parts)
     value = whole_job_rate(step_bytes, args.steps, world, max_seconds) / 1e9
@@ -955,6 +1004,7 @@ def run_ours(args):
     paged_streams = paged_streams_timing(dev)
     widths = width_variants_timing(dev)
     small = small_configs_timing(dev)
+    floor = launch_floor_us(dev)
 
     if rank != 0:
         return
@@ -968,6 +1018,9 @@ def run_ours(args):
                  "frac_of_peak": round(p.nbytes / (us * 1e-6) / 1e9 / peak, 4)}
         if p.name.startswith("prefill"):
             entry["mtok_s"] = round(p.tokens / (us * 1e-6) / 1e6, 1)
+            # launches of this part alone, back to back (inputs exceed L2)
+            entry["us_back_to_back"] = round(b2b[p.name], 2)
+            entry["gbs_back_to_back"] = round(p.nbytes / (b2b[p.name] * 1e-6) / 1e9, 1)
         if p.name == "decode":
             entry["us_per_call_l2_cold"] = round(us, 2)
             entry["us_per_call_graph_warm"] = round(graph_us, 2)
@@ -1003,6 +1056,7 @@ def run_ours(args):
         "paged_streams": paged_streams,
         "width_variants": widths,
         "small_configs": small,
+        "launch_floor_us": floor,
         "parts": parts_out,
         "roofline": {"bound": "hbm", "kernel": dominant.kernel, "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
