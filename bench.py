@@ -285,6 +285,8 @@ def whole_job_rate(units_per_rank_step: float, steps: int, world: int, max_secon
 KERNEL_SOURCE = {
     "fwd_cl_async_kernel": "ccv_fwd.cu",
     "fwd_cf_async_kernel": "ccv_fwd.cu",
+    "fwd_cl_short_kernel": "ccv_fwd.cu",
+    "fwd_cf_short_kernel": "ccv_fwd.cu",
     "update_kernel": "ccv_update.cu",
     "spec_kernel": "ccv_update.cu",
     "paged_row_kernel": "paged_sconv.cu",
