@@ -904,22 +904,16 @@ def back_to_back_us(part, calls=50):
 
 def launch_floor_us(dev, calls=100):
     """The cost of any launch as the parts and the extras are timed: a
-    one-element torch kernel, us per call back to back (events around many
-    calls) and one at a time after an L2 flush (events around each call,
-    the flush outside them), mean of many calls."""
+    one-element torch kernel, us per call one at a time after an L2 flush
+    (events around each call, the flush outside them), and back to back from
+    a CUDA graph of `calls` such launches (so the host's launch cost does not
+    count), means of many calls."""
     tiny = torch.zeros(1, device=dev)
     stream = torch.cuda.current_stream()
+    flush = L2Flush(dev)
     for _ in range(10):
         tiny.add_(1.0)
     torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(calls):
-        tiny.add_(1.0)
-    b.record(stream)
-    torch.cuda.synchronize()
-    b2b = a.elapsed_time(b) * 1e3 / calls
-    flush = L2Flush(dev)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(calls)]
     for e0, e1 in evs:
@@ -929,7 +923,22 @@ def launch_floor_us(dev, calls=100):
         e1.record(stream)
     torch.cuda.synchronize()
     single = sum(e0.elapsed_time(e1) * 1e3 for e0, e1 in evs) / calls
-    return {"back_to_back": round(b2b, 2), "single_after_flush": round(single, 2),
+    s = torch.cuda.Stream()
+    s.wait_stream(stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(calls):
+            tiny.add_(1.0)
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(10):
+        g.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    graphed = a.elapsed_time(b) * 1e3 / (10 * calls)
+    return {"single_after_flush": round(single, 2), "back_to_back_graph": round(graphed, 2),
             "kernel": "one-element torch add"}
 
 
