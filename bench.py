@@ -697,6 +697,51 @@ def paged_streams_timing(dev, calls=100):
             "gbs_fused": round(nbytes / (us_fused * 1e-6) / 1e9, 1)}
 
 
+def paged_single_launch_timing(dev, calls=100):
+    """The paged workload as one paged_sconv_fwd_with_metadata launch (the
+    metadata resolved in the conv kernel) against paged_sconv_seq_metadata +
+    paged_sconv_fwd: us per call L2-cold (L2Flush between calls, outside the
+    timed window), mean of many calls."""
+    import causal_depthwise_conv1d_fwd_gb300 as ccv
+    from causal_depthwise_conv1d_fwd_gb300 import workloads as wl
+
+    c = wl.config_paged()
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in c.kwargs().items()}
+    qsl = c.query_start_loc.to(dev)
+    seq = torch.empty(c.T, dtype=torch.int32, device=dev)
+    qs = torch.empty(c.T, dtype=torch.int32, device=dev)
+    d["seq_idx"], d["query_start"] = seq, qs
+    n_req = len(c.req_lengths)
+    meta = ccv.prepare_paged_sconv_seq_metadata(qsl, n_req, c.num_actual_tokens, seq, qs, c.T)
+    conv = ccv.prepare_paged_sconv_fwd(**d)
+    d1 = {k: v for k, v in d.items() if k not in ("seq_idx", "query_start")}
+    single = ccv.prepare_paged_sconv_fwd_with_metadata(
+        query_start_loc=qsl, num_reqs=n_req, num_actual_tokens=c.num_actual_tokens,
+        seq_idx_out=seq, query_start_out=qs, **d1)
+    stream = torch.cuda.current_stream().cuda_stream
+    flush = L2Flush(dev)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(calls)]
+        for a, b in evs:
+            flush()
+            a.record()
+            fn()
+            b.record()
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) * 1e3 for a, b in evs) / calls
+
+    us_two = timed(lambda: (meta(stream), conv(stream)))
+    us_one = timed(lambda: single(stream))
+    nbytes = paged_bytes(c)
+    return {"workload": c.name, "bytes": nbytes, "us_metadata_then_conv_l2_cold": round(us_two, 2),
+            "us_single_launch_l2_cold": round(us_one, 2),
+            "gbs_single_launch": round(nbytes / (us_one * 1e-6) / 1e9, 1)}
+
+
 def width_variants_timing(dev, calls=20):
     """The large prefill in both layouts for every width 2..5, with bias and
     SiLU and without either (not part of the step).  Inputs are larger than
@@ -1013,6 +1058,7 @@ def run_ours(args):
     spec = spec_verify_timing(dev, rank)
     atrex = atrex_shapes_timing(dev)
     paged_streams = paged_streams_timing(dev)
+    paged_single = paged_single_launch_timing(dev)
     widths = width_variants_timing(dev)
     small = small_configs_timing(dev)
     floor = launch_floor_us(dev)
@@ -1065,6 +1111,7 @@ def run_ours(args):
         "spec_verify": spec,
         "atrex_shapes": atrex,
         "paged_streams": paged_streams,
+        "paged_single_launch": paged_single,
         "width_variants": widths,
         "small_configs": small,
         "launch_floor_us": floor,

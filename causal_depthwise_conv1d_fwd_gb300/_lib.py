@@ -42,6 +42,10 @@ SIGNATURES = {
     "paged_sconv_fwd": ([P, I64, P, I64, I64, I64, I32, I32, I32, I32,
                          P, I64, I64, P, I64, P, P, P, P, I64, I32, I32,
                          P, I32, I32, I32, I32, I32, I32, P, P], I32),
+    "paged_sconv_fwd_with_metadata": ([P, I64, P, I64, I64, I64, I32, I32, I32, I32,
+                                       P, I64, I64, P, I64, P, P, I32, I32, P, P,
+                                       P, P, I64, I32, I32, I32, I32, I32, I32, I32, I32,
+                                       P, P], I32),
     "paged_sconv_fwd_streams": ([P, I32, P, I64, I64, I64, I32, I32, I32, I32,
                                  P, P, P, P, I64, I32, I32, P, I32, I32, I32, I32, P, P], I32),
 }

@@ -371,6 +371,71 @@ def prepare_paged_sconv_fwd(x, weight, cache, positions, block_table, seq_idx, s
                   (x, weight, cache, pos, sidx, slots, block_table, qs, out, err_count))
 
 
+def paged_sconv_fwd_with_metadata(x: torch.Tensor, weight: torch.Tensor, cache: torch.Tensor,
+                                  positions: torch.Tensor, block_table: torch.Tensor,
+                                  query_start_loc: torch.Tensor, num_reqs: int,
+                                  num_actual_tokens: int, slot_mapping: torch.Tensor,
+                                  off_s: int, ws: int, block_size: int, activation=None,
+                                  use_residual: bool = True, out: Optional[torch.Tensor] = None,
+                                  seq_idx_out: Optional[torch.Tensor] = None,
+                                  query_start_out: Optional[torch.Tensor] = None,
+                                  err_count: Optional[torch.Tensor] = None,
+                                  stream=None) -> torch.Tensor:
+    """paged_sconv_fwd in one launch that resolves each token's request and
+    first x-row from query_start_loc itself (and writes them to seq_idx_out
+    / query_start_out when given).  Returns out [T, H*ws]."""
+    return prepare_paged_sconv_fwd_with_metadata(
+        x, weight, cache, positions, block_table, query_start_loc, num_reqs, num_actual_tokens,
+        slot_mapping, off_s, ws, block_size, activation, use_residual, out, seq_idx_out,
+        query_start_out, err_count)(stream)
+
+
+def prepare_paged_sconv_fwd_with_metadata(x, weight, cache, positions, block_table,
+                                          query_start_loc, num_reqs, num_actual_tokens,
+                                          slot_mapping, off_s, ws, block_size, activation=None,
+                                          use_residual=True, out=None, seq_idx_out=None,
+                                          query_start_out=None, err_count=None) -> Launch:
+    """Validate and marshal a paged_sconv_fwd_with_metadata call once."""
+    _need_cuda(x, "x", torch.bfloat16)
+    _need_cuda(weight, "weight", torch.bfloat16)
+    _need_cuda(cache, "cache", torch.bfloat16)
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be [T, C] with channel stride 1")
+    if cache.dim() != 4 or cache.stride(3) != 1:
+        raise ValueError("cache must be [num_blocks, H, N, D] with D stride 1")
+    num_blocks, H, N, D = cache.shape
+    if N != block_size:
+        raise ValueError("block_size does not match the cache's N")
+    T, C = x.shape
+    if C != H * ws or weight.dim() != 2 or weight.shape[0] != C:
+        raise ValueError("x / weight channels must equal H * ws")
+    width = weight.shape[1]
+    pos = _index_vector(positions, "positions", torch.int64, T)
+    slots = _index_vector(slot_mapping, "slot_mapping", torch.int64, T)
+    qsl = _index_vector(query_start_loc, "query_start_loc", torch.int32, num_reqs)
+    seq_o = _index_vector(seq_idx_out, "seq_idx_out", torch.int32, T)
+    qs_o = _index_vector(query_start_out, "query_start_out", torch.int32, T)
+    _need_cuda(block_table, "block_table", torch.int32)
+    if block_table.dim() != 2 or block_table.stride(1) != 1:
+        raise ValueError("block_table must be [num_reqs, max_blocks] with stride 1 along blocks")
+    if out is None:
+        out = torch.empty_like(x)
+    else:
+        _need_cuda(out, "out", torch.bfloat16)
+        if out.shape != x.shape or out.stride(1) != 1:
+            raise ValueError("out must be [T, C] with channel stride 1")
+    _need_cuda(err_count, "err_count", torch.int32)
+    cs = cache.stride()
+    args = (_ptr(x), x.stride(0), _ptr(cache), cs[0], cs[1], cs[2], num_blocks, H, N, D,
+            _ptr(weight), weight.stride(0), weight.stride(1), _ptr(out), out.stride(0),
+            _ptr(pos), _ptr(qsl), num_reqs, num_actual_tokens, _ptr(seq_o), _ptr(qs_o),
+            _ptr(slots), _ptr(block_table), block_table.stride(0), block_table.shape[0],
+            block_table.shape[1], T, off_s, ws, width, _silu_flag(activation),
+            int(bool(use_residual)), _ptr(err_count))
+    return Launch("paged_sconv_fwd_with_metadata", args, out,
+                  (x, weight, cache, pos, qsl, seq_o, qs_o, slots, block_table, out, err_count))
+
+
 def paged_sconv_fwd_streams(streams, cache: torch.Tensor, positions: torch.Tensor,
                             block_table: torch.Tensor, seq_idx: torch.Tensor,
                             slot_mapping: torch.Tensor, query_start: torch.Tensor,

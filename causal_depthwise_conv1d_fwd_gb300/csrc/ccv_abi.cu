@@ -22,4 +22,5 @@ extern "C" const char *ccv_status_string(int status) {
 
 // 1.1.0: ccv_update_spec and paged_sconv_fwd_streams added.
 // 1.2.0: programmatic dependent launches; short-problem prefill kernels.
-extern "C" int ccv_version(void) { return 1 * 10000 + 2 * 100 + 0; }
+// 1.3.0: paged_sconv_fwd_with_metadata added.
+extern "C" int ccv_version(void) { return 1 * 10000 + 3 * 100 + 0; }

@@ -52,6 +52,14 @@ struct PagedArgs {
     int n_shift;  // log2(N) when N is a power of two, else -1
     int w_vec;    // weights contiguous [C, W] and 16-byte aligned
     int *err;
+    // With own_meta the kernel finds each token's request and first x-row
+    // from qsl itself, exactly as paged_sconv_seq_metadata does, instead of
+    // reading seq_idx and qstart, and writes them to seq_out / qs_out when
+    // set.  qsl is read only when num_reqs > 0.
+    int own_meta;
+    const int32_t *qsl;
+    int num_reqs, num_actual;
+    int32_t *seq_out, *qs_out;
 };
 
 // The fields that differ between the conv streams of one layer (each stream
@@ -116,21 +124,77 @@ struct TokenPlan {
     int64_t ins;
 };
 
-// The four per-token index values; a token past T reads as a PAD row.
+// The four per-token index values.
 struct TokenMeta {
     int64_t slot, pos;
     int req, qs;
 };
 
+// Request and first x-row of token t from query_start_loc, with the steps
+// of the metadata kernel: the largest j in [0, num_reqs) with qsl[j] <= t
+// (0 if none) by the same binary search, and qsl[j]; rows from num_actual
+// on get 0 and 0.  Warp-cooperative: every lane of the warp calls it for its
+// own token.  Up to 32 requests lane i holds qsl[i] and the search reads it
+// by shuffle (one round trip for the warp); beyond, each lane searches
+// global memory on its own.
+__device__ __forceinline__ void resolve_request(const PagedArgs &a, int t, bool valid, TokenMeta &m) {
+    const int lane = threadIdx.x & 31;
+    int lo = 0;
+    if (a.num_reqs > 0 && a.num_reqs <= 32) {  // warp-uniform
+        const int q = lane < a.num_reqs ? __ldg(a.qsl + lane) : 0;
+        int hi = a.num_reqs - 1;
+        // A fixed count of steps keeps every lane in the shuffles; five
+        // halvings settle any window of up to 32 entries.
+#pragma unroll
+        for (int step = 0; step < 6; ++step) {
+            const int mid = (lo + hi + 1) >> 1;
+            const int qm = __shfl_sync(kFullMask, q, mid);
+            if (lo < hi) {
+                if (qm <= t) lo = mid;
+                else hi = mid - 1;
+            }
+        }
+        m.qs = __shfl_sync(kFullMask, q, lo);
+    } else if (a.num_reqs > 32) {
+        int hi = a.num_reqs - 1;
+        if (valid && t < a.num_actual) {
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (__ldg(a.qsl + mid) <= t) lo = mid;
+                else hi = mid - 1;
+            }
+            m.qs = __ldg(a.qsl + lo);
+        }
+    }
+    m.req = lo;
+    if (!valid || t >= a.num_actual) {
+        m.req = 0;
+        m.qs = 0;
+    }
+}
+
+// The four per-token index values; a token past T reads as a PAD row.
+// Every lane of the warp calls this (the request search may be shared).
 __device__ __forceinline__ TokenMeta load_meta(const PagedArgs &a, int t, bool valid) {
     TokenMeta m{-1, 0, 0, 0};
     if (valid) {
         m.slot = __ldg(a.slot + t);
         m.pos = __ldg(a.pos + t);
-        m.req = __ldg(a.seq_idx + t);
-        m.qs = __ldg(a.qstart + t);
+        if (!a.own_meta) {
+            m.req = __ldg(a.seq_idx + t);
+            m.qs = __ldg(a.qstart + t);
+        }
     }
+    if (a.own_meta) resolve_request(a, t, valid, m);
     return m;
+}
+
+// Write the token's request and first x-row where the caller asked for them
+// (one channel block per token writes).
+__device__ __forceinline__ void store_meta(const PagedArgs &a, int t, bool valid, const TokenMeta &m) {
+    if (!valid) return;
+    if (a.seq_out != nullptr) a.seq_out[t] = m.req;
+    if (a.qs_out != nullptr) a.qs_out[t] = m.qs;
 }
 
 // Lane l of a warp resolves the plan of token t (one lane per token), so the
@@ -213,7 +277,9 @@ __global__ void __launch_bounds__(kThreads) paged_scalar_kernel(const PagedArgs 
 #pragma unroll
     for (int u = 0; u < kRun; ++u) xg[u] = active && t0 + u < t1 ? __ldg(a.x + (t0 + u) * a.xs_t + c0) : 0;
 
-    const TokenPlan<W> mine = plan_token<W>(a, t0 + lane, load_meta(a, t0 + lane, t0 + lane < t1));
+    const TokenMeta meta = load_meta(a, t0 + lane, t0 + lane < t1);
+    if (blockIdx.y == 0) store_meta(a, t0 + lane, t0 + lane < t1, meta);
+    const TokenPlan<W> mine = plan_token<W>(a, t0 + lane, meta);
 
     const int head = active ? c0 / a.ws : 0;
     const int64_t chan_off = static_cast<int64_t>(head) * a.cs_h + a.off_s + (active ? c0 % a.ws : 0);
@@ -382,6 +448,7 @@ __global__ void __launch_bounds__(kRowMaxThreads, 8) paged_row_kernel(const Page
         if (m % kStageGroup == kStageGroup - 1 || m == R - 1) cp_async_commit();
     }
     if (tid < 32) {
+        if (blockIdx.y == 0 && blockIdx.z == 0) store_meta(a, t0 + tid, tid < n, meta);
         // Lane u plans token t0 + u; lanes past the run carry an empty plan.
         const TokenPlan<W> p = plan_token<W>(a, t0 + tid, meta);
         if (tid < kRowRun) {
@@ -562,6 +629,11 @@ struct PagedShared {
     const int32_t *qstart;
     int T, width, silu, residual;
     int *err;
+    // set for the single-launch call that resolves the metadata itself
+    int own_meta = 0;
+    const int32_t *qsl = nullptr;
+    int num_reqs = 0, num_actual = 0;
+    int32_t *seq_out = nullptr, *qs_out = nullptr;
 };
 
 int check_shared(const PagedShared &p) {
@@ -607,6 +679,12 @@ PagedArgs shared_args(const PagedShared &p) {
     a.T = p.T;
     a.n_shift = (p.N & (p.N - 1)) == 0 ? __builtin_ctz(static_cast<unsigned>(p.N)) : -1;
     a.err = p.err;
+    a.own_meta = p.own_meta;
+    a.qsl = p.qsl;
+    a.num_reqs = p.num_reqs;
+    a.num_actual = p.num_actual;
+    a.seq_out = p.seq_out;
+    a.qs_out = p.qs_out;
     return a;
 }
 
@@ -709,9 +787,9 @@ int paged_run(const PagedShared &p, const ccv_paged_stream *streams, int n, ccv_
         }
     }
     if (p.T == 0) return CCV_OK;
-    if (p.cache == nullptr || p.pos == nullptr || p.seq_idx == nullptr || p.slot == nullptr ||
-        p.bt == nullptr || p.qstart == nullptr)
+    if (p.cache == nullptr || p.pos == nullptr || p.slot == nullptr || p.bt == nullptr)
         return CCV_ERR_NULL_POINTER;
+    if (!p.own_meta && (p.seq_idx == nullptr || p.qstart == nullptr)) return CCV_ERR_NULL_POINTER;
     const Extent ec = cache_extent(p);
     for (int i = 0; i < n; ++i) {
         const ccv_paged_stream &st = streams[i];
@@ -772,4 +850,32 @@ extern "C" int paged_sconv_fwd_streams(const ccv_paged_stream *streams, int num_
                              positions, seq_idx, slot_mapping, block_table, bt_stride_r, bt_rows,
                              max_blocks, query_start, T, width, silu, residual, err_count};
     return ccv::paged_run(p, streams, num_streams, stream);
+}
+
+extern "C" int paged_sconv_fwd_with_metadata(
+    const void *x, int64_t x_stride_t, void *cache, int64_t c_stride_blk, int64_t c_stride_h,
+    int64_t c_stride_n, int num_blocks, int H, int N, int D, const void *weight,
+    int64_t w_stride_c, int64_t w_stride_w, void *out, int64_t out_stride_t,
+    const int64_t *positions, const int32_t *query_start_loc, int num_reqs,
+    int num_actual_tokens, int32_t *seq_idx_out, int32_t *query_start_out,
+    const int64_t *slot_mapping, const int32_t *block_table, int64_t bt_stride_r, int bt_rows,
+    int max_blocks, int T, int off_s, int ws, int width, int silu, int residual, int *err_count,
+    ccv_stream_t stream) {
+    using namespace ccv;
+    if (num_reqs < 0 || num_actual_tokens < 0 || T < 0) return CCV_ERR_SIZE;
+    if (num_actual_tokens > T) return CCV_ERR_SIZE;
+    if (num_reqs == 0 && num_actual_tokens > 0) return CCV_ERR_SIZE;
+    if (T > 0 && num_reqs > 0 && query_start_loc == nullptr) return CCV_ERR_NULL_POINTER;
+    PagedShared p{cache, c_stride_blk, c_stride_h, c_stride_n, num_blocks, H, N, D,
+                  positions, nullptr, slot_mapping, block_table, bt_stride_r, bt_rows,
+                  max_blocks, nullptr, T, width, silu, residual, err_count};
+    p.own_meta = 1;
+    p.qsl = query_start_loc;
+    p.num_reqs = num_reqs;
+    p.num_actual = num_actual_tokens;
+    p.seq_out = seq_idx_out;
+    p.qs_out = query_start_out;
+    const ccv_paged_stream st{x, x_stride_t, weight, w_stride_c, w_stride_w, out, out_stride_t,
+                              off_s, ws};
+    return paged_run(p, &st, 1, stream);
 }

@@ -238,6 +238,40 @@ int paged_sconv_fwd(const void *x, int64_t x_stride_t,
                     ccv_stream_t stream);
 
 /*
+ * paged_sconv_fwd_with_metadata -- paged_sconv_fwd in one launch, with the
+ * token metadata resolved inside it.  vLLM Inkling sconv.py,
+ * `sconv_seq_metadata` / `_seq_metadata_kernel` and `fused_sconv` /
+ * `_fused_sconv_kernel`: each token's request and first x-row are computed
+ * from query_start_loc exactly as paged_sconv_seq_metadata computes them,
+ * then the insert and conv run as in paged_sconv_fwd.
+ *
+ * query_start_loc, num_reqs, num_actual_tokens  as for
+ *               paged_sconv_seq_metadata, with T the padded token count:
+ *               num_actual_tokens <= T, and num_reqs == 0 only with no real
+ *               token (CCV_ERR_SIZE otherwise).
+ * seq_idx_out, query_start_out  int32 [T] each, or NULL: when given they
+ *               receive the metadata (the same values paged_sconv_seq_metadata
+ *               writes), so that later calls of the same forward -- other
+ *               layers, other streams -- can pass them to paged_sconv_fwd.
+ *               They must not overlap any other argument.
+ * Every other argument means what it means for paged_sconv_fwd.  out, the
+ * cache and err_count end up as after paged_sconv_seq_metadata followed by
+ * paged_sconv_fwd.
+ */
+int paged_sconv_fwd_with_metadata(const void *x, int64_t x_stride_t,
+                                  void *cache, int64_t c_stride_blk, int64_t c_stride_h,
+                                  int64_t c_stride_n, int num_blocks, int H, int N, int D,
+                                  const void *weight, int64_t w_stride_c, int64_t w_stride_w,
+                                  void *out, int64_t out_stride_t,
+                                  const int64_t *positions, const int32_t *query_start_loc,
+                                  int num_reqs, int num_actual_tokens,
+                                  int32_t *seq_idx_out, int32_t *query_start_out,
+                                  const int64_t *slot_mapping, const int32_t *block_table,
+                                  int64_t bt_stride_r, int bt_rows, int max_blocks,
+                                  int T, int off_s, int ws, int width, int silu, int residual,
+                                  int *err_count, ccv_stream_t stream);
+
+/*
  * One conv stream of a layer for paged_sconv_fwd_streams: its input, its
  * weights, its output and the D-range [off_s, off_s + ws) of the shared
  * cache it owns.  Fields mean what the same-named arguments of

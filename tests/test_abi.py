@@ -32,7 +32,7 @@ def test_every_declared_function_is_exported(lib):
     names = _lib.declared_functions()
     assert set(names) == {"ccv_status_string", "ccv_version", "ccv_fwd", "ccv_update",
                           "ccv_update_spec", "paged_sconv_seq_metadata", "paged_sconv_fwd",
-                          "paged_sconv_fwd_streams"}
+                          "paged_sconv_fwd_with_metadata", "paged_sconv_fwd_streams"}
     out = subprocess.run(["nm", "-D", "--defined-only", build.LIB], capture_output=True,
                          text=True, check=True).stdout
     exported = set(re.findall(r" T (\w+)$", out, flags=re.M))
@@ -47,7 +47,7 @@ def test_status_strings(lib):
         s = _lib.status_string(code)
         assert s and "unknown" not in s
     assert "unknown" in _lib.status_string(-1000)
-    assert lib.ccv_version() == 10200
+    assert lib.ccv_version() == 10300
 
 
 def fwd(lib, **over):
@@ -269,3 +269,25 @@ def test_binding_rejects_a_strided_or_misshapen_bias():
         api._bias_vector(torch.zeros(15), 16)
     # a single channel has no stride to get wrong
     assert api._bias_vector(packed[:1, 2], 1) is not None
+
+
+def paged_meta(lib, **over):
+    args = dict(x=A, xst=2048, cache=B, csb=16 * 16 * 512, csh=16 * 512, csn=512, nb=1024, H=16,
+                N=16, D=512, w=C, wsc=4, wsw=1, out=C + 65536, ost=2048, pos=C + 2 * 65536,
+                qsl=C + 3 * 65536, nreq=3, nact=8, seqo=None, qso=None, slot=C + 4 * 65536,
+                bt=C + 5 * 65536, btr=200, btrows=32, maxb=200, T=8, off_s=128, ws=128, width=4,
+                silu=1, resid=1, err=None, stream=None)
+    args.update(over)
+    return lib.paged_sconv_fwd_with_metadata(*args.values())
+
+
+def test_paged_with_metadata_validation(lib):
+    assert paged_meta(lib, nact=9) == SIZE     # more real tokens than rows
+    assert paged_meta(lib, nreq=0) == SIZE     # real tokens but no request
+    assert paged_meta(lib, nreq=-1) == SIZE
+    assert paged_meta(lib, qsl=None) == NULLP
+    assert paged_meta(lib, width=9) == WIDTH
+    assert paged_meta(lib, off_s=400) == RANGE
+    assert paged_meta(lib, out=A + 16) == ALIAS
+    assert paged_meta(lib, bt=None) == NULLP
+    assert paged_meta(lib, T=0, nact=0) == OK

@@ -51,6 +51,10 @@ def fresh():
     st["qsl"] = pg.query_start_loc.to(dev)
     st["seq"] = torch.zeros(pg.T, dtype=torch.int32, device=dev)
     st["qs"] = torch.zeros(pg.T, dtype=torch.int32, device=dev)
+    st["pg3"] = {k: v for k, v in to_dev(pg).items() if k not in ("seq_idx", "query_start")}
+    st["pg3_out"] = torch.empty_like(st["pg3"]["x"])
+    st["seq3"] = torch.zeros(pg.T, dtype=torch.int32, device=dev)
+    st["qs3"] = torch.zeros(pg.T, dtype=torch.int32, device=dev)
     return st
 
 def run(st, s=None):
@@ -61,6 +65,10 @@ def run(st, s=None):
     ccv.paged_sconv_seq_metadata(st["qsl"], len(pg.req_lengths), pg.num_actual_tokens,
                                  st["seq"], st["qs"], pg.T, stream=s)
     ccv.paged_sconv_fwd(**st["pg"], out=st["pg_out"], stream=s)
+    ccv.paged_sconv_fwd_with_metadata(query_start_loc=st["qsl"], num_reqs=len(pg.req_lengths),
+                                      num_actual_tokens=pg.num_actual_tokens,
+                                      seq_idx_out=st["seq3"], query_start_out=st["qs3"],
+                                      out=st["pg3_out"], stream=s, **st["pg3"])
     return ccv.paged_sconv_fwd_streams(st["streams"], st["cache2"], block_size=pg.block_size,
                                        activation="silu", use_residual=True, stream=s,
                                        **st["meta"])
@@ -91,6 +99,10 @@ same(g_state["spec"]["conv_state"], e_state["spec"]["conv_state"], "spec pool")
 same(g_state["spec"]["intermediate_conv_window"], e_state["spec"]["intermediate_conv_window"], "spec windows")
 same(g_state["pg_out"], e_state["pg_out"], "paged out")
 same(g_state["pg"]["cache"], e_state["pg"]["cache"], "paged cache")
+same(g_state["pg3_out"], e_state["pg3_out"], "single-launch paged out")
+same(g_state["pg3"]["cache"], e_state["pg3"]["cache"], "single-launch paged cache")
+if not (torch.equal(g_state["seq3"], e_state["seq3"]) and torch.equal(g_state["qs3"], e_state["qs3"])):
+    raise SystemExit("graph vs eager differ: single-launch metadata")
 for i in range(2):
     same(g_outs[i], e_outs[i], f"stream {i} out")
 same(g_state["cache2"], e_state["cache2"], "streams cache")
