@@ -72,10 +72,11 @@ __device__ __forceinline__ Raw<VEC> gather(const uint16_t *p, int64_t stride, bo
 
 // Stores of outputs, state lines and windows.  Vector stores carry the
 // streaming (evict-first) hint: what a decode step writes is read again only
-// at the next step, after other work has passed through L2, and marked
-// evict-first its dirty lines are written back while the memory system is
-// idle in this latency-bound kernel's wake rather than during the streaming
-// prefill that follows in a mixed step (1% faster per step, measured).
+// at the next step, after other work has passed through L2.  In a mixed step
+// (prefill, decode, paged conv, then prefill again) the hint made the whole
+// step 1% faster without changing this kernel's own time (measured); the
+// likely cause is that the lines marked evict-first are written back before
+// the streaming prefill needs the bandwidth.
 template <int VEC>
 __device__ __forceinline__ void scatter(uint16_t *p, int64_t stride, bool vec, const Raw<VEC> &r) {
     if (VEC == 8 && vec) {
