@@ -395,3 +395,19 @@ def test_automatic_choice_at_its_threshold(prefill_path, monkeypatch, layout, to
     if names is not None:
         want = "short" if tokens * 4096 <= (1 << 23) else "async"
         assert any(want in n for n in names), names
+
+
+@pytest.mark.parametrize("layout", ["tokens_dim", "dim_tokens"])
+@pytest.mark.parametrize("batch", [33, 100, 1100])
+def test_many_sequences(layout, batch):
+    """More than 32 sequences: the chunk search narrows the candidates in
+    rounds before its final one (one round up to 1024 sequences, two past
+    it), with zero-length and pad sequences among them."""
+    import random
+
+    r = random.Random(1800 + batch)
+    lengths = [r.choice([0, 1, 2, 3, 5, 9, 17, r.randint(1, 60)]) for _ in range(batch)]
+    pads = tuple(i for i in range(batch) if r.random() < 0.1)
+    case = wl.varlen_prefill(1800 + batch, lengths, 16, 4, num_cache_lines=batch + 3,
+                             layout=layout, pad_positions=pads, has_init="bernoulli")
+    check(case)
