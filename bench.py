@@ -987,6 +987,40 @@ def launch_floor_us(dev, calls=100):
             "kernel": "one-element torch add"}
 
 
+def copy_same_size_timing(x, calls=50):
+    """A torch copy of the prefill input into a second buffer of the same
+    size (the same bytes read and written as a prefill launch moves, minus
+    the states and weights): us per copy back to back, and one at a time
+    with events around each copy as the parts loop times its parts.  Both
+    L2-cold: the two buffers exceed L2."""
+    y = torch.empty_like(x)
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        y.copy_(x)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(calls):
+        y.copy_(x)
+    b.record(stream)
+    torch.cuda.synchronize()
+    b2b = a.elapsed_time(b) * 1e3 / calls
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(calls)]
+    for e0, e1 in evs:
+        e0.record(stream)
+        y.copy_(x)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    single = sum(e0.elapsed_time(e1) * 1e3 for e0, e1 in evs) / calls
+    nbytes = 2 * x.numel() * x.element_size()
+    del y
+    return {"bytes": nbytes, "us_back_to_back": round(b2b, 2),
+            "gbs_back_to_back": round(nbytes / (b2b * 1e-6) / 1e9, 1),
+            "us_event_bracketed": round(single, 2),
+            "gbs_event_bracketed": round(nbytes / (single * 1e-6) / 1e9, 1)}
+
+
 def concurrent_streams_timing(parts, steps):
     """The step's parts on two streams at once: the prefill parts on one,
     decode and paged on another (they share no buffer), as an engine would
@@ -1097,6 +1131,7 @@ def run_ours(args):
     widths = width_variants_timing(dev)
     small = small_configs_timing(dev)
     floor = launch_floor_us(dev)
+    copy_ref = copy_same_size_timing(dev_args["prefill_tokens_dim"][0]["x"])
 
     if rank != 0:
         return
@@ -1105,14 +1140,22 @@ def run_ours(args):
     parts_out = {}
     for p in parts:
         us = p.ms * 1e3 / args.steps
+        # What one launch moving these bytes at the copy rate would take when
+        # timed the same way: the launch floor plus bytes / peak.
+        ref_us = floor["single_after_flush"] + p.nbytes / (peak * 1e3)
         entry = {"kernel": p.kernel, "us": round(us, 2), "bytes": p.nbytes,
                  "gbs": round(p.nbytes / (us * 1e-6) / 1e9, 1),
-                 "frac_of_peak": round(p.nbytes / (us * 1e-6) / 1e9 / peak, 4)}
+                 "frac_of_peak": round(p.nbytes / (us * 1e-6) / 1e9 / peak, 4),
+                 "launch_floor_plus_copy_us": round(ref_us, 2),
+                 "frac_of_launch_floor_plus_copy": round(ref_us / us, 4)}
         if p.name.startswith("prefill"):
             entry["mtok_s"] = round(p.tokens / (us * 1e-6) / 1e6, 1)
             # launches of this part alone, back to back (inputs exceed L2)
             entry["us_back_to_back"] = round(b2b[p.name], 2)
             entry["gbs_back_to_back"] = round(p.nbytes / (b2b[p.name] * 1e-6) / 1e9, 1)
+            # against a torch copy of x (same size), each timed the same way
+            entry["frac_of_same_size_copy_back_to_back"] = round(copy_ref["us_back_to_back"] / b2b[p.name], 4)
+            entry["frac_of_same_size_copy_event_bracketed"] = round(copy_ref["us_event_bracketed"] / us, 4)
         if p.name == "decode":
             entry["us_per_call_l2_cold"] = round(us, 2)
             entry["us_per_call_graph_warm"] = round(graph_us, 2)
@@ -1151,6 +1194,7 @@ def run_ours(args):
         "width_variants": widths,
         "small_configs": small,
         "launch_floor_us": floor,
+        "copy_same_size": copy_ref,
         "parts": parts_out,
         "roofline": {"bound": "hbm", "kernel": dominant.kernel, "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
