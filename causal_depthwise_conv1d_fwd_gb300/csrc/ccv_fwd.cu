@@ -660,7 +660,10 @@ __global__ void __launch_bounds__(kCaThreads, W == 5 ? 2 : 3) fwd_cl_async_kerne
 // The 4 tokens before a lane's vector come from lane l-1 by shuffle (lane 0:
 // lane 31 of the previous segment).  Taps are native bf16 x bf16 + fp32
 // FMAs on the packed 12-token window; segments wholly inside the chunk run
-// without per-lane checks.
+// without per-lane checks.  Outputs are written with plain stores, not the
+// evict-first hint of the channel-last kernel: with plain stores the prefill
+// parts and the whole step ran 1.7% faster (measured; for the channel-last
+// kernel the hint is the faster choice).
 
 constexpr int kCfaThreads = 256;
 constexpr int kCfaWarps = kCfaThreads / 32;
@@ -672,6 +675,8 @@ constexpr size_t kCfaSmem = sizeof(uint4) * kCfaSlots * kCfaThreads;
 static_assert(kCfaChunk + kMaxWidth - 1 + kCfaAlign - 1 <= kCfaSegs * 256, "a chunk must fit its segments");
 // Segment 1 must start after the chunk's first token (it runs unchecked).
 static_assert(256 - (kCfaAlign - 1) - (kMaxWidth - 1) > 0, "segment 1 must lie inside the chunk");
+
+__device__ __forceinline__ void cfa_store(uint16_t *p, const uint4 &v) { *reinterpret_cast<uint4 *>(p) = v; }
 
 // The 8 logical inputs at tokens t0..t0+7 of one row: x inside [lo, cend),
 // the prior (packed, oldest first) just before a sequence's first chunk, 0
@@ -860,7 +865,7 @@ __global__ void __launch_bounds__(kCfaThreads, 4) fwd_cf_async_kernel(const FwdA
         if (t0 + 8 <= cbeg || t0 >= cend) return;
         const uint4 o = cfa_outputs<W, SILU>(E, wt, bs);
         if (t0 >= cbeg && t0 + 8 <= cend) {
-            __stcs(reinterpret_cast<uint4 *>(oc + t0), o);
+            cfa_store(oc + t0, o);
         } else {
             const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
@@ -891,7 +896,7 @@ __global__ void __launch_bounds__(kCfaThreads, 4) fwd_cf_async_kernel(const FwdA
             const uint4 v = ring_base[((1 + u) % kCfaSlots) * kCfaThreads];
             cp_async16(ring_base + u * kCfaThreads, nxt + u * 256);
             cp_async_commit();
-            if (u > 0 || have) __stcs(reinterpret_cast<uint4 *>(dst + (u - 1) * 256), pend);
+            if (u > 0 || have) cfa_store(dst + (u - 1) * 256, pend);
             uint32_t E[6];
             window(v, E);
             pend = cfa_outputs<W, SILU>(E, wt, bs);
@@ -900,7 +905,7 @@ __global__ void __launch_bounds__(kCfaThreads, 4) fwd_cf_async_kernel(const FwdA
         nxt += kCfaSlots * 256;
         dst += kCfaSlots * 256;
     }
-    if (have) __stcs(reinterpret_cast<uint4 *>(dst - 256), pend);
+    if (have) cfa_store(dst - 256, pend);
     for (; j + kCfaSlots - 1 < jin1; ++j) {
         cp_async_wait<kCfaSlots - 2>();
         const uint4 v = ring_base[(j % kCfaSlots) * kCfaThreads];
@@ -909,7 +914,7 @@ __global__ void __launch_bounds__(kCfaThreads, 4) fwd_cf_async_kernel(const FwdA
         nxt += 256;
         uint32_t E[6];
         window(v, E);
-        __stcs(reinterpret_cast<uint4 *>(dst), cfa_outputs<W, SILU>(E, wt, bs));
+        cfa_store(dst, cfa_outputs<W, SILU>(E, wt, bs));
         dst += 256;
     }
     // Interior segments whose streamed-in successor may cross the chunk's
@@ -921,7 +926,7 @@ __global__ void __launch_bounds__(kCfaThreads, 4) fwd_cf_async_kernel(const FwdA
         cp_async_commit();
         uint32_t E[6];
         window(v, E);
-        __stcs(reinterpret_cast<uint4 *>(dst), cfa_outputs<W, SILU>(E, wt, bs));
+        cfa_store(dst, cfa_outputs<W, SILU>(E, wt, bs));
         dst += 256;
     }
     for (; j < nseg; ++j) step_checked(j);
