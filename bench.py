@@ -40,7 +40,7 @@ import torch  # noqa: E402
 
 METRIC = "varlen causal_conv1d HBM GB/s & Mtok/s at dim 8192 bf16; decode us/call"
 WORKLOAD = ("prefill 4x4096 tokens dim 8192 W4 (tokens,dim) + same in (dim,tokens) "
-            "+ decode 256x8192 + paged short conv H16 ws128 32 requests")
+            "+ paged short conv H16 ws128 32 requests + decode 256x8192")
 
 
 # ----------------------------------------------------------- byte counts ----
@@ -358,7 +358,13 @@ class Part:
 
 
 def make_parts(dev, rank):
-    """The four parts of a step as pre-marshalled launches on the current stream."""
+    """The four parts of a step as pre-marshalled launches on the current stream,
+    in step order: the two prefill layouts, then paged, then decode.  The
+    parts share no buffer, so any order computes the same; the order sets
+    which launch absorbs which predecessor's pending writes.  Over all six
+    cyclic orders the step measured 194.1-207.8 us on one box: the two
+    prefill launches side by side, then paged, then decode, is within 0.3 us
+    of the fastest (and 1.7 us faster than decode before paged)."""
     import causal_depthwise_conv1d_fwd_gb300 as ccv
     from causal_depthwise_conv1d_fwd_gb300 import workloads as wl
 
@@ -380,11 +386,6 @@ def make_parts(dev, rank):
         launch = ccv.prepare_ccv_fwd(**d, out=out)
         parts.append(Part(name, "fwd_cl_async_kernel" if name.endswith("tokens_dim") else "fwd_cf_async_kernel",
                           1, prefill_bytes(c), prefill_tokens(c), launch, stream))
-    c = cases["decode"]
-    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in c.kwargs().items()}
-    dev_args["decode"] = (d, d["x"])
-    launch = ccv.prepare_ccv_update(**d)
-    parts.append(Part("decode", "update_kernel", 1, decode_bytes(c), c.x.shape[0], launch, stream))
     c = cases["paged"]
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in c.kwargs().items()}
     qsl = c.query_start_loc.to(dev)
@@ -402,6 +403,11 @@ def make_parts(dev, rank):
         conv(handle)
 
     parts.append(Part("paged", "paged_row_kernel", 2, paged_bytes(c), c.T, paged_step, stream))
+    c = cases["decode"]
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in c.kwargs().items()}
+    dev_args["decode"] = (d, d["x"])
+    launch = ccv.prepare_ccv_update(**d)
+    parts.append(Part("decode", "update_kernel", 1, decode_bytes(c), c.x.shape[0], launch, stream))
     return parts, cases, dev_args
 
 
@@ -427,13 +433,6 @@ def run_e2e(dev, cases, dev_args, steps):
         plan.append((name, d, out, hx, ho))
         h2d += hx.numel() * 2
         d2h += ho.numel() * 2
-    d, out = dev_args["decode"]
-    hx = pinned_like(d["x"])
-    hx.copy_(cases["decode"].x)
-    ho = pinned_like(out)
-    plan.append(("decode", d, out, hx, ho))
-    h2d += hx.numel() * 2
-    d2h += ho.numel() * 2
     d, out = dev_args["paged"]
     c = cases["paged"]
     hx = pinned_like(d["x"])
@@ -444,6 +443,13 @@ def run_e2e(dev, cases, dev_args, steps):
     qsl_dev = torch.empty_like(hq, device=dev)
     plan.append(("paged", d, out, hx, ho))
     h2d += hx.numel() * 2 + sum(v.numel() * v.element_size() for v in hmeta.values()) + hq.numel() * 4
+    d2h += ho.numel() * 2
+    d, out = dev_args["decode"]
+    hx = pinned_like(d["x"])
+    hx.copy_(cases["decode"].x)
+    ho = pinned_like(out)
+    plan.append(("decode", d, out, hx, ho))
+    h2d += hx.numel() * 2
     d2h += ho.numel() * 2
 
     # Copy-in streams, a compute stream and copy-out streams.  Part i's
