@@ -70,17 +70,16 @@ __device__ __forceinline__ Raw<VEC> gather(const uint16_t *p, int64_t stride, bo
     return r;
 }
 
-// Stores of outputs, state lines and windows.  Vector stores carry the
-// streaming (evict-first) hint: what a decode step writes is read again only
-// at the next step, after other work has passed through L2.  In a mixed step
-// (prefill, decode, paged conv, then prefill again) the hint made the whole
-// step 1% faster without changing this kernel's own time (measured); the
-// likely cause is that the lines marked evict-first are written back before
-// the streaming prefill needs the bandwidth.
+// Stores of outputs, state lines and windows: plain stores.  The streaming
+// (evict-first) hint was measured both ways: with decode right after the
+// channel-first prefill (whose stores then carried the hint too) it made the
+// whole step 1% faster, and in the step as the bench now runs it (prefill in
+// both layouts, paged conv, decode) 0.35% slower; neither changes this
+// kernel's own time.
 template <int VEC>
 __device__ __forceinline__ void scatter(uint16_t *p, int64_t stride, bool vec, const Raw<VEC> &r) {
     if (VEC == 8 && vec) {
-        store_stream<VEC>(p, r);
+        store_plain<VEC>(p, r);
     } else {
 #pragma unroll
         for (int v = 0; v < VEC; ++v) p[v * stride] = r.elem(v);
