@@ -9,7 +9,8 @@ decode (256 x 8192; prefill parts take --width), paged (H16 x ws128, 32 requests
 spec (speculative verify, 64 rows x 4 drafts, dim 8192), atrex (one
 channel-first sequence of --tokens x --dim, the atrex-bench #003 shapes),
 paged_streams (a layer's four conv streams on one paged cache, one launch),
-varlen (8 sequences of 1..512 tokens, dim 4096, channel-last).
+varlen (8 sequences of 1..512 tokens, dim 4096, channel-last), paged_single
+(the paged workload as one paged_sconv_fwd_with_metadata launch).
 The process exits 0 after a device synchronize; it times nothing.
 """
 from __future__ import annotations
@@ -22,7 +23,7 @@ from . import api
 from . import workloads as wl
 
 PARTS = ("prefill_tokens_dim", "prefill_dim_tokens", "decode", "paged", "spec", "atrex",
-         "paged_streams", "varlen")
+         "paged_streams", "varlen", "paged_single")
 
 
 def _dev(kwargs, dev):
@@ -62,6 +63,15 @@ def make_launch(part: str, dev, tokens: int = 1024, dim: int = 4096, width: int 
             meta()
             conv()
         return run
+    if part == "paged_single":
+        c = wl.config_paged()
+        d = {k: v for k, v in _dev(c.kwargs(), dev).items() if k not in ("seq_idx", "query_start")}
+        seq = torch.empty(c.T, dtype=torch.int32, device=dev)
+        qs = torch.empty(c.T, dtype=torch.int32, device=dev)
+        launch = api.prepare_paged_sconv_fwd_with_metadata(
+            query_start_loc=c.query_start_loc.to(dev), num_reqs=len(c.req_lengths),
+            num_actual_tokens=c.num_actual_tokens, seq_idx_out=seq, query_start_out=qs, **d)
+        return lambda: launch()
     if part == "spec":
         c = wl.config_spec_decode()
         d = _dev(c.kwargs(), dev)
