@@ -362,9 +362,9 @@ def make_parts(dev, rank):
     in step order: the two prefill layouts, then paged, then decode.  The
     parts share no buffer, so any order computes the same; the order sets
     which launch absorbs which predecessor's pending writes.  Over all six
-    cyclic orders the step measured 194.1-207.8 us on one box: the two
-    prefill launches side by side, then paged, then decode, is within 0.3 us
-    of the fastest (and 1.7 us faster than decode before paged)."""
+    cyclic orders the step measured 191.6-201.2 us on one box: the two
+    prefill launches side by side, then paged, then decode, is within 0.1 us
+    of the fastest (decode before paged is the slowest)."""
     import causal_depthwise_conv1d_fwd_gb300 as ccv
     from causal_depthwise_conv1d_fwd_gb300 import workloads as wl
 
