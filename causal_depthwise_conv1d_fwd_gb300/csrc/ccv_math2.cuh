@@ -32,11 +32,6 @@ __device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
     return d;
 }
 
-// bf16x2 word -> (lo, hi) fp32 pair (exact).
-__device__ __forceinline__ f32x2 widen2(uint32_t w) {
-    return pack2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-}
-
 // acc + lo(x) * lo(w) and acc + hi(x) * hi(w) with bf16 sources and fp32
 // accumulators (one rounding each; the bf16 product is exact in fp32, so this
 // equals the fp32 fma of the widened values).
