@@ -56,6 +56,15 @@ MUTANTS = [
      "const int shift = 0;"),
     ("spec_output_column_shifted", "conv_state[o * ss_line + c * ss_dim + j * ss_tok] = v;",
      "conv_state[o * ss_line + c * ss_dim + (j + 1) * ss_tok] = v;"),
+    ("update_bias_dropped", "float bc = bias ? bf16_to_f32(bias[c]) : 0.0f;", "float bc = 0.0f;"),
+    ("silu_ignores_flag", "if (silu) acc = silu_f32(acc);", "acc = silu_f32(acc);"),
+    ("metadata_pad_rows_take_last_request",
+     "            seq_idx_out[t] = 0;\n            query_start_out[t] = 0;",
+     "            seq_idx_out[t] = num_reqs - 1;\n            query_start_out[t] = 0;"),
+    ("decode_pad_counted_as_error",
+     "        if (line == pad_slot_id) continue;\n        if (line < 0 || line >= num_cache_lines) {",
+     "        if (line < 0 || line >= num_cache_lines) {"),
+    ("paged_taps_reversed", "weight[c * ws_c + iw * ws_w]", "weight[c * ws_c + (W - 1 - iw) * ws_w]"),
 ]
 
 
