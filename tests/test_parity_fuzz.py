@@ -57,6 +57,42 @@ def test_fwd_random(seed, monkeypatch):
         assert_bits(d["conv_states"], ref_states, f"{case.name} states")
 
 
+@pytest.mark.parametrize("seed", range(60))
+def test_decode_random(seed):
+    """ccv_update without the spec extras: one or more tokens per row, both
+    state layouts, wider states, PAD rows, no index vector, in place or into
+    a separate out, bias and SiLU on or off, odd and vector dims."""
+    r = random.Random(7300 + seed)
+    width = r.randint(2, 5)
+    batch = r.randint(1, 40)
+    seqlen = r.choice([1, 1, 1, 2, 3])
+    dim = r.choice([8, 16, 64, 1024, 1032, 13, 100, 8192])
+    extra = r.choice([0, 0, 1, 3])
+    with_indices = r.random() < 0.8
+    case = wl.decode(9100 + seed, batch, dim, width, seqlen=seqlen,
+                     state_len=width - 2 + seqlen + extra,
+                     state_layout=r.choice(["dim_contiguous", "tok_contiguous"]),
+                     pad_positions=(tuple(i for i in range(batch) if r.random() < 0.15)
+                                    if with_indices else ()),
+                     use_bias=r.random() < 0.7, activation=r.choice(["silu", None]),
+                     with_indices=with_indices, squeeze=r.random() < 0.7,
+                     name=f"fuzz_decode_{seed}")
+    separate = r.random() < 0.3
+    ref_state = case.conv_state.clone()
+    ref_buf = torch.full_like(case.x, -3.0) if separate else None
+    ref_out, _ = oracle.ccv_update(case.x.clone(), ref_state, case.weight, case.bias,
+                                   case.activation, case.conv_state_indices, case.pad_slot_id,
+                                   out=ref_buf)
+    d = to_device(case.kwargs(), DEV)
+    buf = torch.full_like(d["x"], -3.0) if separate else None
+    out = ccv.ccv_update(**d, out=buf)
+    torch.cuda.synchronize()
+    assert_close(out, ref_out, case.name)
+    assert_bits(d["conv_state"], ref_state, f"{case.name} conv_state")
+    if separate:
+        assert_bits(d["x"], case.x, f"{case.name} x unchanged")
+
+
 @pytest.mark.parametrize("seed", range(80))
 def test_update_random(seed):
     r = random.Random(7100 + seed)
