@@ -682,10 +682,17 @@ __global__ void __launch_bounds__(kCaThreads, W == 5 ? 2 : 3) fwd_cl_async_kerne
 // evict-first hint of the channel-last kernel: with plain stores the prefill
 // parts and the whole step ran 1.7% faster (measured; for the channel-last
 // kernel the hint is the faster choice).
+//
+// The grid has total_tokens / kCfaChunk + batch chunk slots per row group,
+// an upper bound the host can compute without reading query_start_loc; the
+// surplus slots exit after the chunk search.  Long chunks (128 segments,
+// 32632 tokens) keep the surplus small: 32-segment chunks left a third of
+// the blocks empty on 4 x 4096 tokens and split 11027-token sequences into
+// uneven pairs (measured: 83.4 -> 82.1 us and 67.7 -> 59.7 us).
 
 constexpr int kCfaThreads = 256;
 constexpr int kCfaWarps = kCfaThreads / 32;
-constexpr int kCfaSegs = 32;
+constexpr int kCfaSegs = 128;
 constexpr int kCfaAlign = 128;  // tokens: segments start on a 256-byte boundary
 constexpr int kCfaChunk = kCfaSegs * 256 - kCfaAlign - 8;  // + halo (<= 4) + alignment (< 128)
 constexpr int kCfaSlots = 8;

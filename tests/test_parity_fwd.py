@@ -5,7 +5,7 @@ choice on both sides of its size threshold.
 Outputs within 1e-2*|ref| + 2e-5, conv_state bit-exact, untouched regions
 (pad sequences, zero-length sequences, wider state columns, guard bands)
 bit-exact.  Sizes span several chunks and ragged tails of both kernels
-(channel-last chunks of 256 tokens; channel-first chunks of 8056 tokens for
+(channel-last chunks of 256 tokens; channel-first chunks of 32632 tokens for
 aligned rows and 256 for the strided fallback).
 """
 from __future__ import annotations
@@ -17,6 +17,7 @@ import oracle
 import causal_depthwise_conv1d_fwd_gb300 as ccv
 from causal_depthwise_conv1d_fwd_gb300 import workloads as wl
 from parity_util import assert_bits, assert_close, sentinel_like, to_device
+from test_kernel_tiling import K as TILING
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda", 0)
@@ -138,10 +139,12 @@ def test_dims_not_multiple_of_eight(dim, layout):
 @pytest.mark.parametrize("extra", [0, 3])
 def test_channel_first_chunk_edges(width, extra):
     """Sequences one token short of, exactly at and one past the channel-first
-    chunk length (8056 tokens) and of two chunks, on rows at several 16-byte
-    phases: the second chunk's halo and segment 0's slack (up to 127 tokens
-    before the first one needed) meet the previous chunk's last segment."""
-    case = wl.varlen_prefill(520 + width + extra, [8055, 8056, 8057, 16113, 3], 8, width,
+    chunk length (kCfaChunk, read from the kernel source) and of two chunks,
+    on rows at several 16-byte phases: the second chunk's halo and segment
+    0's slack (up to 127 tokens before the first one needed) meet the
+    previous chunk's last segment."""
+    c = TILING["kCfaChunk"]
+    case = wl.varlen_prefill(520 + width + extra, [c - 1, c, c + 1, 2 * c + 1, 3], 8, width,
                              num_cache_lines=6, layout="dim_tokens", has_init="all",
                              extra_tokens=extra)
     check(case)
