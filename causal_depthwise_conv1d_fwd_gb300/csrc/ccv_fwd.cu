@@ -683,18 +683,23 @@ __global__ void __launch_bounds__(kCaThreads, W == 5 ? 2 : 3) fwd_cl_async_kerne
 // parts and the whole step ran 1.7% faster (measured; for the channel-last
 // kernel the hint is the faster choice).
 //
-// The grid has total_tokens / kCfaChunk + batch chunk slots per row group,
-// an upper bound the host can compute without reading query_start_loc; the
-// surplus slots exit after the chunk search.  Long chunks (128 segments,
-// 32632 tokens) keep the surplus small: 32-segment chunks left a third of
-// the blocks empty on 4 x 4096 tokens and split 11027-token sequences into
-// uneven pairs (measured: 83.4 -> 82.1 us and 67.7 -> 59.7 us).
+// The chunk length CHUNK is chosen on the host from total_tokens and batch
+// (cf_long_chunks) and the grid has total_tokens / CHUNK + batch chunk slots
+// per row group, an upper bound computed without reading query_start_loc;
+// the surplus slots exit after the chunk search.  Sequences of up to 16384
+// tokens on average take one kCfaChunk-token chunk (128 segments) each and
+// leave few surplus slots (8056-token chunks left a third of the blocks
+// empty on 4 x 4096 tokens and split 11027-token sequences unevenly:
+// 83.4 -> 82.1 us and 67.7 -> 59.7 us, measured); longer sequences keep
+// 8056-token chunks (one 32632-token chunk plus a short one took 1 x 40000
+// tokens from 197 to 214 us).
 
 constexpr int kCfaThreads = 256;
 constexpr int kCfaWarps = kCfaThreads / 32;
 constexpr int kCfaSegs = 128;
 constexpr int kCfaAlign = 128;  // tokens: segments start on a 256-byte boundary
 constexpr int kCfaChunk = kCfaSegs * 256 - kCfaAlign - 8;  // + halo (<= 4) + alignment (< 128)
+constexpr int kCfaChunkSplit = 32 * 256 - kCfaAlign - 8;      // 8056: chunks of long sequences
 constexpr int kCfaSlots = 8;
 constexpr size_t kCfaSmem = sizeof(uint4) * kCfaSlots * kCfaThreads;
 static_assert(kCfaChunk + kMaxWidth - 1 + kCfaAlign - 1 <= kCfaSegs * 256, "a chunk must fit its segments");
@@ -787,21 +792,21 @@ __device__ __forceinline__ uint4 cfa_outputs(const uint32_t (&E)[6], const uint3
     return make_uint4(ow[0], ow[1], ow[2], ow[3]);
 }
 
-template <int W, bool SILU>
+template <int W, bool SILU, int CHUNK>
 __global__ void __launch_bounds__(kCfaThreads, 4) fwd_cf_async_kernel(const FwdArgs a) {
     extern __shared__ __align__(16) uint4 s_ring[];  // [kCfaSlots][kCfaThreads]
     wait_prior_grid();  // no early release: see the note on the streaming kernels' launches
     validate_sequence(a);
     ChunkInfo ci;
-    if (!locate_chunk(a, kCfaChunk, blockIdx.x, ci)) return;
+    if (!locate_chunk(a, CHUNK, blockIdx.x, ci)) return;
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int c = blockIdx.y * kCfaWarps + (tid >> 5);
     if (c >= a.dim) return;  // warp-uniform
 
     const uint16_t *const xc = a.x + c * a.xs_d;
-    const int cbeg = ci.start + ci.chunk * kCfaChunk;
-    const int cend = ci.start + min(ci.len, (ci.chunk + 1) * kCfaChunk);
+    const int cbeg = ci.start + ci.chunk * CHUNK;
+    const int cend = ci.start + min(ci.len, (ci.chunk + 1) * CHUNK);
     const bool chunk0 = ci.chunk == 0;
     const int lo = chunk0 ? cbeg : cbeg - (W - 1);
     // where the row starts within its 256-byte block of memory, in tokens
@@ -1322,6 +1327,18 @@ KernelFn pick_kernel(int width, bool silu) {
     return nullptr;
 }
 
+// Chunk length of the channel-first streaming kernel, from the sizes alone
+// (the grid must not depend on query_start_loc): sequences of at most
+// kCfaOneChunk tokens on average take one kCfaChunk-token chunk each, so few
+// surplus slots remain; longer ones are cut into kCfaChunkSplit-token
+// chunks, so no block streams a very long row.  The length is a template
+// argument: as a runtime value the kernel measured 2.3 us slower.
+constexpr int kCfaOneChunk = 16384;
+
+bool cf_long_chunks(int total, int batch) {
+    return (static_cast<int64_t>(total) + batch - 1) / batch <= kCfaOneChunk;
+}
+
 template <int W, bool SILU>
 int launch_cl_async_w(const FwdArgs &a, cudaStream_t stream) {
     int dev = 0;
@@ -1336,17 +1353,23 @@ int launch_cl_async_w(const FwdArgs &a, cudaStream_t stream) {
                       dim3(kCaThreads), kCaSmem, stream, a);
 }
 
-template <int W, bool SILU>
-int launch_cf_async_w(const FwdArgs &a, cudaStream_t stream) {
+template <int W, bool SILU, int CHUNK>
+int launch_cf_async_chunk(const FwdArgs &a, cudaStream_t stream) {
     int dev = 0;
     current_device_sms(&dev);
     cudaError_t e;
-    if (resident_blocks<fwd_cf_async_kernel<W, SILU>>(kCfaThreads, kCfaSmem, dev, &e) == 0)
+    if (resident_blocks<fwd_cf_async_kernel<W, SILU, CHUNK>>(kCfaThreads, kCfaSmem, dev, &e) == 0)
         return static_cast<int>(e);
-    const dim3 grid(static_cast<unsigned>(a.total / kCfaChunk + a.batch),
+    const dim3 grid(static_cast<unsigned>(a.total / CHUNK + a.batch),
                     static_cast<unsigned>((a.dim + kCfaWarps - 1) / kCfaWarps));
     if (grid.y > 65535u) return CCV_ERR_SIZE;
-    return launch_pdl(fwd_cf_async_kernel<W, SILU>, grid, dim3(kCfaThreads), kCfaSmem, stream, a);
+    return launch_pdl(fwd_cf_async_kernel<W, SILU, CHUNK>, grid, dim3(kCfaThreads), kCfaSmem, stream, a);
+}
+
+template <int W, bool SILU>
+int launch_cf_async_w(const FwdArgs &a, cudaStream_t stream) {
+    return cf_long_chunks(a.total, a.batch) ? launch_cf_async_chunk<W, SILU, kCfaChunk>(a, stream)
+                                            : launch_cf_async_chunk<W, SILU, kCfaChunkSplit>(a, stream);
 }
 
 template <int W, bool SILU>

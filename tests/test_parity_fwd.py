@@ -10,6 +10,8 @@ aligned rows and 256 for the strided fallback).
 """
 from __future__ import annotations
 
+import os
+
 import pytest
 import torch
 
@@ -143,11 +145,42 @@ def test_channel_first_chunk_edges(width, extra):
     on rows at several 16-byte phases: the second chunk's halo and segment
     0's slack (up to 127 tokens before the first one needed) meet the
     previous chunk's last segment."""
-    c = TILING["kCfaChunk"]
-    case = wl.varlen_prefill(520 + width + extra, [c - 1, c, c + 1, 2 * c + 1, 3], 8, width,
+    lengths = _lengths_around_cf_chunk()
+    case = wl.varlen_prefill(520 + width + extra, lengths, 8, width,
                              num_cache_lines=6, layout="dim_tokens", has_init="all",
                              extra_tokens=extra)
     check(case)
+
+
+def _cf_chunk_tokens(total, batch):
+    """The host's choice of channel-first chunk length (cf_long_chunks in the
+    kernel source), with its constants read from the source."""
+    import re
+
+    src = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                            "causal_depthwise_conv1d_fwd_gb300", "csrc", "ccv_fwd.cu")).read()
+    one = int(re.search(r"constexpr int kCfaOneChunk = (\d+);", src).group(1))
+    split_expr = re.search(r"constexpr int kCfaChunkSplit = ([^;]+);", src).group(1)
+    split = int(eval(split_expr, {"__builtins__": {}}, {"kCfaAlign": TILING["kCfaAlign"]}))
+    avg = -(-total // batch)
+    return TILING["kCfaChunk"] if avg <= one else split
+
+
+def _lengths_around_cf_chunk():
+    """Sequence lengths c-1, c, c+1, 2c+1 and 3 around the chunk length c the
+    host picks for long sequences, plus a filler sequence that makes the
+    average long enough for that choice."""
+    c = _cf_chunk_tokens(1 << 20, 1)
+    head = [c - 1, c, c + 1, 2 * c + 1, 3]
+    return head + [70000]
+
+
+def test_chunk_edge_lengths_sit_on_the_chosen_chunk():
+    """The chunk-edge cases above straddle the chunk length the host picks."""
+    lengths = _lengths_around_cf_chunk()
+    c = lengths[1]
+    assert _cf_chunk_tokens(sum(lengths), len(lengths)) == c
+    assert c < TILING["kCfaChunk"]  # the split chunk, not one chunk per sequence
 
 
 @pytest.mark.parametrize("extra", [0, 1, 3, 5])
