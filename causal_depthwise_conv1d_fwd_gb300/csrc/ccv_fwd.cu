@@ -172,6 +172,81 @@ __device__ __forceinline__ bool sequence_line(const FwdArgs &a, const ChunkInfo 
     return true;
 }
 
+struct SeqChunk {
+    int seq, chunk, start, len, line;
+    bool init;
+};
+
+// Slot -> (sequence, chunk) as locate_chunk, plus the sequence's state line
+// and has_initial_state flag, in one round trip for up to 32 * PER
+// sequences: lane l of the final round loads candidates PER*l .. PER*l+PER-1
+// of the window (their offsets, lines and flags together), and the winner's
+// are shuffled to every lane.  false for a surplus slot, a pad or invalid
+// line, or bad offsets.
+template <int PER>
+__device__ __forceinline__ bool locate_seq(const FwdArgs &a, int chunk_tokens, int slot, SeqChunk &sc) {
+    const int lane = threadIdx.x & 31;
+    int lo = 0, n = a.batch;
+    while (n > 32 * PER) {  // narrow to at most 32 * PER candidates
+        const int stride = (n + 31) >> 5;
+        const int off = lane * stride;
+        bool le = false;
+        if (off < n) {
+            const int i = lo + off;
+            le = floor_div(__ldg(a.qsl + i), chunk_tokens) + i <= slot;
+        }
+        const unsigned m = __ballot_sync(kFullMask, le);
+        if (m == 0u) return false;
+        const int top = 31 - __clz(m);
+        lo += top * stride;
+        n = min(stride, n - top * stride);
+    }
+    const int base = PER * lane;  // this lane's first candidate, from lo
+    int s[PER + 1], line[PER], init[PER];
+#pragma unroll
+    for (int k = 0; k <= PER; ++k) s[k] = base + k <= n ? __ldg(a.qsl + lo + base + k) : 0;
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+        const int i = lo + base + k;
+        const bool in = base + k < n;
+        line[k] = in ? (a.cidx ? __ldg(a.cidx + i) : i) : 0;
+        init[k] = in && a.has_init != nullptr ? a.has_init[i] : 0;
+    }
+    int pick = -1;  // this lane's last candidate at or before the slot
+#pragma unroll
+    for (int k = 0; k < PER; ++k)
+        if (base + k < n && floor_div(s[k], chunk_tokens) + lo + base + k <= slot) pick = k;
+    const unsigned m = __ballot_sync(kFullMask, pick >= 0);
+    if (m == 0u) return false;
+    const int top = 31 - __clz(m);
+    int ps = 0, pe = 0, pl = 0, pi = 0;
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+        if (k == pick) {
+            ps = s[k];
+            pe = s[k + 1];
+            pl = line[k];
+            pi = init[k];
+        }
+    }
+    sc.seq = lo + PER * top + __shfl_sync(kFullMask, pick, top);
+    sc.start = __shfl_sync(kFullMask, ps, top);
+    const int end = __shfl_sync(kFullMask, pe, top);
+    sc.line = __shfl_sync(kFullMask, pl, top);
+    sc.init = a.st != nullptr && __shfl_sync(kFullMask, pi, top) != 0;
+    if (sc.start < 0 || end < sc.start || end > a.total) return false;
+    const int k = slot - (sc.start / chunk_tokens + sc.seq);
+    if (k < 0 || static_cast<int64_t>(k) * chunk_tokens >= end - sc.start) return false;
+    if (sc.line == a.pad) return false;
+    if (a.st != nullptr && (sc.line < 0 || sc.line >= a.num_lines)) return false;
+    sc.chunk = k;
+    sc.len = end - sc.start;
+    return true;
+}
+__device__ __forceinline__ bool locate_short(const FwdArgs &a, int chunk_tokens, int slot, SeqChunk &sc) {
+    return locate_seq<1>(a, chunk_tokens, slot, sc);
+}
+
 template <int VEC>
 __device__ __forceinline__ Raw<VEC> load_state(const FwdArgs &a, int line, int c0, int col) {
     const uint16_t *p = a.st + line * a.ss_l + c0 * a.ss_d + col * a.ss_t;
@@ -673,8 +748,14 @@ __global__ void __launch_bounds__(kCaThreads, W == 5 ? 2 : 3) fwd_cl_async_kerne
 // faster than 16-byte alignment, measured).  Lane l owns tokens 8l..8l+7
 // of a segment.  Each lane streams its 16-byte vectors through a private
 // ring of kCfaSlots shared-memory slots with cp.async, started as soon as
-// the chunk is known (a vector that crosses the chunk's edge is assembled
-// with scalar loads, the prior included, and stored into the slot instead).
+// the chunk is known, edge segments included: the tokens outside the chunk
+// that a vector carries feed no stored output, and the W-1 tokens before a
+// sequence's first chunk take the prior when segment 0 is read.  The chunk
+// search returns the sequence's state line and flag with its offsets in one
+// round trip for up to 128 sequences, so the prior and the x entries of the
+// new state load while the ring fills (with the edges assembled from scalar
+// loads after the prior and the search taking up to three round trips, 64
+// sequences of 1024 tokens ran at half the copy rate).
 // The 4 tokens before a lane's vector come from lane l-1 by shuffle (lane 0:
 // lane 31 of the previous segment).  Taps are native bf16 x bf16 + fp32
 // FMAs on the packed 12-token window; segments wholly inside the chunk run
@@ -701,6 +782,7 @@ constexpr int kCfaAlign = 128;  // tokens: segments start on a 256-byte boundary
 constexpr int kCfaChunk = kCfaSegs * 256 - kCfaAlign - 8;  // + halo (<= 4) + alignment (< 128)
 constexpr int kCfaChunkSplit = 32 * 256 - kCfaAlign - 8;      // 8056: chunks of long sequences
 constexpr int kCfaSlots = 8;
+constexpr int kCfaPer = 4;  // sequences per lane in the chunk search: one round trip up to 128
 constexpr size_t kCfaSmem = sizeof(uint4) * kCfaSlots * kCfaThreads;
 static_assert(kCfaChunk + kMaxWidth - 1 + kCfaAlign - 1 <= kCfaSegs * 256, "a chunk must fit its segments");
 // Segment 1 must start after the chunk's first token (it runs unchecked).
@@ -708,12 +790,10 @@ static_assert(256 - (kCfaAlign - 1) - (kMaxWidth - 1) > 0, "segment 1 must lie i
 
 __device__ __forceinline__ void cfa_store(uint16_t *p, const uint4 &v) { *reinterpret_cast<uint4 *>(p) = v; }
 
-// The 8 logical inputs at tokens t0..t0+7 of one row: x inside [lo, cend),
-// the prior (packed, oldest first) just before a sequence's first chunk, 0
-// elsewhere.  Only vectors at a chunk's edges take this path.
-template <int W>
-__device__ __noinline__ uint4 cfa_edge_vector(const uint16_t *xc, int t0, int lo, int cbeg, int cend,
-                                              bool chunk0, uint32_t prior01, uint32_t prior23) {
+// The 8 inputs at tokens t0..t0+7 of one row where the 16-byte vector
+// crosses an end of the row (rows that do not start on a 16-byte boundary):
+// x inside [0, total), 0 outside.
+__device__ __noinline__ uint4 cfa_ragged_vector(const uint16_t *xc, int t0, int total) {
     uint32_t w[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -721,17 +801,32 @@ __device__ __noinline__ uint4 cfa_edge_vector(const uint16_t *xc, int t0, int lo
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const int t = t0 + 2 * q + e;
-            uint32_t val = 0;
-            if (t >= lo && t < cend) {
-                val = xc[t];
-            } else if (chunk0 && t >= cbeg - (W - 1) && t < cbeg) {
-                const int i = t - cbeg + (W - 1);  // prior column
-                const uint32_t src = i < 2 ? prior01 : prior23;
-                val = (i & 1) ? (src >> 16) : (src & 0xffffu);
-            }
-            pair |= val << (16 * e);
+            if (t >= 0 && t < total) pair |= uint32_t(xc[t]) << (16 * e);
         }
         w[q] = pair;
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// A sequence's first chunk: tokens cbeg-(W-1) .. cbeg-1 of the vector at
+// t0 take the prior (its W-1 columns packed oldest first, 0 without an
+// initial state) in place of the x of whatever precedes the sequence.
+template <int W>
+__device__ __forceinline__ uint4 cfa_with_prior(const uint4 &v, int t0, int cbeg, uint32_t prior01,
+                                                uint32_t prior23) {
+    if (t0 + 8 <= cbeg - (W - 1) || t0 >= cbeg) return v;
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int i = t0 + 2 * q + e - cbeg + (W - 1);  // prior column
+            if (i >= 0 && i < W - 1) {
+                const uint32_t src = i < 2 ? prior01 : prior23;
+                const uint32_t val = (i & 1) ? (src >> 16) : (src & 0xffffu);
+                w[q] = (w[q] & (0xffff0000u >> (16 * e))) | (val << (16 * e));
+            }
+        }
     }
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
@@ -797,18 +892,18 @@ __global__ void __launch_bounds__(kCfaThreads, 4) fwd_cf_async_kernel(const FwdA
     extern __shared__ __align__(16) uint4 s_ring[];  // [kCfaSlots][kCfaThreads]
     wait_prior_grid();  // no early release: see the note on the streaming kernels' launches
     validate_sequence(a);
-    ChunkInfo ci;
-    if (!locate_chunk(a, CHUNK, blockIdx.x, ci)) return;
+    SeqChunk sc;  // the chunk, its sequence's state line and flag: one round trip
+    if (!locate_seq<kCfaPer>(a, CHUNK, blockIdx.x, sc)) return;
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int c = blockIdx.y * kCfaWarps + (tid >> 5);
     if (c >= a.dim) return;  // warp-uniform
 
     const uint16_t *const xc = a.x + c * a.xs_d;
-    const int cbeg = ci.start + ci.chunk * CHUNK;
-    const int cend = ci.start + min(ci.len, (ci.chunk + 1) * CHUNK);
-    const bool chunk0 = ci.chunk == 0;
-    const int lo = chunk0 ? cbeg : cbeg - (W - 1);
+    const int cbeg = sc.start + sc.chunk * CHUNK;
+    const int cend = sc.start + min(sc.len, (sc.chunk + 1) * CHUNK);
+    const bool chunk0 = sc.chunk == 0;
+    const bool keep = chunk0 && a.st != nullptr;  // this chunk reads and writes the state line
     // where the row starts within its 256-byte block of memory, in tokens
     const int phase = static_cast<int>((reinterpret_cast<uintptr_t>(xc) >> 1) & (kCfaAlign - 1));
     // first token of segment 0: aligned, at or before the first token needed
@@ -820,47 +915,38 @@ __global__ void __launch_bounds__(kCfaThreads, 4) fwd_cf_async_kernel(const FwdA
     const int jin1 = max(1, (cend - a0) / 256);
     uint4 *const ring_base = s_ring + tid;
 
-    // Start streaming the segments that lie wholly inside the chunk right
-    // away; segment 0 and the chunk's tail are assembled once the prior is
-    // known.  Segment j goes to slot j % kCfaSlots.
-#pragma unroll
-    for (int j = 1; j < kCfaSlots - 1; ++j) {
-        if (j < jin1) cp_async16(ring_base + j * kCfaThreads, xc + a0 + j * 256 + lane * 8);
-    }
-    int line;
-    if (!sequence_line(a, ci, line)) {
-        cp_async_commit();  // nothing may still land in this block's shared memory
-        cp_async_wait<0>();
-        return;
-    }
-    uint32_t prior01 = 0, prior23 = 0;  // prior columns 0..3, packed
-    if (chunk0 && a.st != nullptr) {
-        // The flag and the state columns are loaded together (neither
-        // depends on the other); the columns count only when the flag is set.
-        const bool init = a.has_init != nullptr && a.has_init[ci.seq] != 0;
-        const uint16_t *sp = a.st + line * a.ss_l + c * a.ss_d;
-        uint32_t p[4] = {0, 0, 0, 0};
-#pragma unroll
-        for (int j = 0; j < W - 1; ++j) p[j] = sp[j * a.ss_t];
-        if (init) {
-            prior01 = p[0] | (p[1] << 16);
-            prior23 = p[2] | (p[3] << 16);
-        }
-    }
-    auto issue_checked = [&](int seg) {
+    // Every segment streams in whole: the tokens of a vector outside the
+    // chunk feed no stored output, except the W-1 before a sequence's first
+    // chunk, which take the prior when segment 0 is read.  Only a vector
+    // that crosses an end of the row is assembled with scalar loads.
+    auto issue = [&](int seg) {
         if (seg >= nseg) return;
         const int t0 = a0 + seg * 256 + lane * 8;
         uint4 *slot = ring_base + (seg % kCfaSlots) * kCfaThreads;
-        if (t0 >= lo && t0 + 8 <= cend) cp_async16(slot, xc + t0);
-        else *slot = cfa_edge_vector<W>(xc, t0, lo, cbeg, cend, chunk0, prior01, prior23);
+        if (t0 >= 0 && t0 + 8 <= a.total) cp_async16(slot, xc + t0);
+        else *slot = cfa_ragged_vector(xc, t0, a.total);
     };
-    // Segments 0..kCfaSlots-2 form one commit group each, in order.
-    issue_checked(0);
-    cp_async_commit();
+    // Segments 0..kCfaSlots-2 form one commit group each, in order; segment
+    // j goes to slot j % kCfaSlots.
 #pragma unroll
-    for (int j = 1; j < kCfaSlots - 1; ++j) {
-        if (j >= jin1) issue_checked(j);  // edge segments not started above
+    for (int j = 0; j < kCfaSlots - 1; ++j) {
+        issue(j);
         cp_async_commit();
+    }
+    // The prior and the x entries of the new state load while the ring fills.
+    uint32_t prior01 = 0, prior23 = 0;  // prior columns 0..3, packed
+    uint16_t xnew = 0;                  // lane < W-1: x entry of new state column lane
+    if (keep) {
+        if (sc.init) {
+            const uint16_t *sp = a.st + sc.line * a.ss_l + c * a.ss_d;
+            uint32_t p[4] = {0, 0, 0, 0};
+#pragma unroll
+            for (int j = 0; j < W - 1; ++j) p[j] = sp[j * a.ss_t];
+            prior01 = p[0] | (p[1] << 16);
+            prior23 = p[2] | (p[3] << 16);
+        }
+        const int idx = sc.len + lane;
+        if (lane < W - 1 && idx >= W - 1) xnew = xc[sc.start + idx - (W - 1)];
     }
 
     uint32_t wt[W];  // tap k's bf16 weight in both halves
@@ -886,12 +972,13 @@ __global__ void __launch_bounds__(kCfaThreads, 4) fwd_cf_async_kernel(const FwdA
     };
     auto step_checked = [&](int j) {
         cp_async_wait<kCfaSlots - 2>();
-        const uint4 v = ring_base[(j % kCfaSlots) * kCfaThreads];
-        issue_checked(j + kCfaSlots - 1);
+        uint4 v = ring_base[(j % kCfaSlots) * kCfaThreads];
+        issue(j + kCfaSlots - 1);
         cp_async_commit();
+        const int t0 = a0 + j * 256 + lane * 8;
+        if (j == 0 && chunk0) v = cfa_with_prior<W>(v, t0, cbeg, prior01, prior23);
         uint32_t E[6];
         window(v, E);
-        const int t0 = a0 + j * 256 + lane * 8;
         if (t0 + 8 <= cbeg || t0 >= cend) return;
         const uint4 o = cfa_outputs<W, SILU>(E, wt, bs);
         if (t0 >= cbeg && t0 + 8 <= cend) {
@@ -952,7 +1039,7 @@ __global__ void __launch_bounds__(kCfaThreads, 4) fwd_cf_async_kernel(const FwdA
     for (; j < jin1; ++j) {
         cp_async_wait<kCfaSlots - 2>();
         const uint4 v = ring_base[(j % kCfaSlots) * kCfaThreads];
-        issue_checked(j + kCfaSlots - 1);
+        issue(j + kCfaSlots - 1);
         cp_async_commit();
         uint32_t E[6];
         window(v, E);
@@ -961,21 +1048,17 @@ __global__ void __launch_bounds__(kCfaThreads, 4) fwd_cf_async_kernel(const FwdA
     }
     for (; j < nseg; ++j) step_checked(j);
 
-    if (chunk0 && a.st != nullptr) {
+    if (keep) {
         // New state = last W-1 entries of prior ++ x[sequence]; the prior was
         // read by every lane above, before any lane writes the line.
-        uint16_t nb = 0;
-        if (lane < W - 1) {
-            const int idx = ci.len + lane;
-            if (idx < W - 1) {
-                const uint32_t src = idx < 2 ? prior01 : prior23;
-                nb = uint16_t((idx & 1) ? (src >> 16) : (src & 0xffffu));
-            } else {
-                nb = xc[ci.start + idx - (W - 1)];
-            }
+        uint16_t nb = xnew;
+        const int idx = sc.len + lane;
+        if (idx < W - 1) {
+            const uint32_t src = idx < 2 ? prior01 : prior23;
+            nb = uint16_t((idx & 1) ? (src >> 16) : (src & 0xffffu));
         }
         __syncwarp();
-        if (lane < W - 1) a.st[line * a.ss_l + c * a.ss_d + lane * a.ss_t] = nb;
+        if (lane < W - 1) a.st[sc.line * a.ss_l + c * a.ss_d + lane * a.ss_t] = nb;
     }
 }
 
@@ -999,61 +1082,6 @@ constexpr int kShortSegs = 5;  // channel-first: 256-token segments per warp
 // 16-byte boundary at or before the chunk's first token covers it
 constexpr int kShortCfChunk = kShortSegs * 256 - 8;
 
-struct ShortChunk {
-    int seq, chunk, start, len, line;
-    bool init;
-};
-
-// Slot -> (sequence, chunk) as locate_chunk, plus the sequence's state line
-// and has_initial_state flag: lane j of the final round loads candidate j's
-// offsets, line and flag together, and the winner's are shuffled to every
-// lane.  false for a surplus slot, a pad or invalid line, or bad offsets.
-__device__ __forceinline__ bool locate_short(const FwdArgs &a, int chunk_tokens, int slot,
-                                             ShortChunk &sc) {
-    const int lane = threadIdx.x & 31;
-    int lo = 0, n = a.batch;
-    while (n > 32) {  // narrow to at most 32 candidates
-        const int stride = (n + 31) >> 5;
-        const int off = lane * stride;
-        bool le = false;
-        if (off < n) {
-            const int i = lo + off;
-            le = floor_div(__ldg(a.qsl + i), chunk_tokens) + i <= slot;
-        }
-        const unsigned m = __ballot_sync(kFullMask, le);
-        if (m == 0u) return false;
-        const int top = 31 - __clz(m);
-        lo += top * stride;
-        n = min(stride, n - top * stride);
-    }
-    int s = 0, e = 0, line = 0, init = 0;
-    bool le = false;
-    if (lane < n) {
-        const int i = lo + lane;
-        s = __ldg(a.qsl + i);
-        e = __ldg(a.qsl + i + 1);
-        line = a.cidx ? __ldg(a.cidx + i) : i;
-        init = a.has_init != nullptr ? a.has_init[i] : 0;
-        le = floor_div(s, chunk_tokens) + i <= slot;
-    }
-    const unsigned m = __ballot_sync(kFullMask, le);
-    if (m == 0u) return false;
-    const int top = 31 - __clz(m);
-    sc.seq = lo + top;
-    sc.start = __shfl_sync(kFullMask, s, top);
-    const int end = __shfl_sync(kFullMask, e, top);
-    sc.line = __shfl_sync(kFullMask, line, top);
-    sc.init = a.st != nullptr && __shfl_sync(kFullMask, init, top) != 0;
-    if (sc.start < 0 || end < sc.start || end > a.total) return false;
-    const int k = slot - (sc.start / chunk_tokens + sc.seq);
-    if (k < 0 || static_cast<int64_t>(k) * chunk_tokens >= end - sc.start) return false;
-    if (sc.line == a.pad) return false;
-    if (a.st != nullptr && (sc.line < 0 || sc.line >= a.num_lines)) return false;
-    sc.chunk = k;
-    sc.len = end - sc.start;
-    return true;
-}
-
 // Channel-last: warp = (run of kShortRun tokens, 256-channel tile), lane =
 // 8 channels; global warp g = slot * tiles + tile.  Every input row of the
 // run goes to shared memory by asynchronous copies (no registers held while
@@ -1075,7 +1103,7 @@ __global__ void __launch_bounds__(kShortThreads, 7) fwd_cl_short_kernel(const Fw
     const int slot = g / ntiles;
     if (slot >= nslots) return;  // warp-uniform
     validate_sequence_at(a, slot, tile == 0 && lane == 0);
-    ShortChunk sc;
+    SeqChunk sc;
     if (!locate_short(a, kShortRun, slot, sc)) return;
     const int c0 = tile * 256 + lane * 8;
     if (c0 >= a.dim) return;
@@ -1222,7 +1250,7 @@ __global__ void __launch_bounds__(kShortThreads) fwd_cf_short_kernel(const FwdAr
     const int c = blockIdx.y * kShortWarps + (threadIdx.x >> 5);
     validate_sequence_at(a, slot, blockIdx.y == 0 && threadIdx.x == 0);
     if (c >= a.dim) return;  // warp-uniform
-    ShortChunk sc;
+    SeqChunk sc;
     if (!locate_short(a, kShortCfChunk, slot, sc)) return;
 
     const uint16_t *const xc = a.x + c * a.xs_d;

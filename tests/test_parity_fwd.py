@@ -434,11 +434,14 @@ def test_automatic_choice_at_its_threshold(prefill_path, monkeypatch, layout, to
 
 
 @pytest.mark.parametrize("layout", ["tokens_dim", "dim_tokens"])
-@pytest.mark.parametrize("batch", [33, 100, 1100])
+@pytest.mark.parametrize("batch", [33, 100, 128, 129, 1100, 4200])
 def test_many_sequences(layout, batch):
     """More than 32 sequences: the chunk search narrows the candidates in
-    rounds before its final one (one round up to 1024 sequences, two past
-    it), with zero-length and pad sequences among them."""
+    rounds before its final one (the short kernels and the channel-last
+    streaming kernel take 32 candidates in the final round, the channel-first
+    streaming kernel 128, four per lane: 128 and 129 sit on its edge, 4200
+    takes it two narrowing rounds), with zero-length and pad sequences among
+    them."""
     import random
 
     r = random.Random(1800 + batch)
