@@ -796,6 +796,43 @@ def width_variants_timing(dev, calls=20):
     return rows
 
 
+SHORT_SEQUENCE_MIXES = ((64, 1024), (256, 256), (16, 2048))
+
+
+def short_sequences_timing(dev, calls=20):
+    """Many short sequences at dim 8192, width 4, bias and SiLU, in both
+    layouts (not part of the step): channel-first takes the multi-row kernel
+    here.  Inputs are larger than L2, so calls run back to back; us per call
+    is the mean of `calls` calls."""
+    import causal_depthwise_conv1d_fwd_gb300 as ccv
+    from causal_depthwise_conv1d_fwd_gb300 import workloads as wl
+
+    stream = torch.cuda.current_stream().cuda_stream
+    rows = []
+    for batch, tokens in SHORT_SEQUENCE_MIXES:
+        for layout in ("tokens_dim", "dim_tokens"):
+            c = wl.varlen_prefill(1010, [tokens] * batch, 8192, 4, layout=layout, has_init="all")
+            d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in c.kwargs().items()}
+            out = torch.empty_strided(d["x"].shape, d["x"].stride(), dtype=torch.bfloat16,
+                                      device=dev)
+            launch = ccv.prepare_ccv_fwd(**d, out=out)
+            for _ in range(3):
+                launch(stream)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(calls):
+                launch(stream)
+            b.record()
+            torch.cuda.synchronize()
+            us = a.elapsed_time(b) * 1e3 / calls
+            nbytes = prefill_bytes(c)
+            rows.append({"sequences": batch, "tokens_each": tokens, "layout": layout,
+                         "us": round(us, 2), "gbs": round(nbytes / (us * 1e-6) / 1e9, 1)})
+            del d, out, launch
+        torch.cuda.empty_cache()
+    return rows
+
+
 def small_configs_timing(dev, calls=100):
     """The single-sequence (dim 64, 16 tokens) and varlen continuous-batching
     (8 sequences, dim 4096) prefill configurations, not part of the step: us
@@ -1138,6 +1175,7 @@ def run_ours(args):
     paged_streams = paged_streams_timing(dev)
     paged_single = paged_single_launch_timing(dev)
     widths = width_variants_timing(dev)
+    short_seqs = short_sequences_timing(dev)
     small = small_configs_timing(dev)
     floor = launch_floor_us(dev)
     copy_ref = copy_same_size_timing(dev_args["prefill_tokens_dim"][0]["x"])
@@ -1201,6 +1239,7 @@ def run_ours(args):
         "paged_streams": paged_streams,
         "paged_single_launch": paged_single,
         "width_variants": widths,
+        "short_sequences": short_seqs,
         "small_configs": small,
         "launch_floor_us": floor,
         "copy_same_size": copy_ref,

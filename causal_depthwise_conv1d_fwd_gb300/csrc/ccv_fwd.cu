@@ -1062,6 +1062,198 @@ __global__ void __launch_bounds__(kCfaThreads, 4) fwd_cf_async_kernel(const FwdA
     }
 }
 
+// ------------------------------- channel-first, cp.async, short chunks ----
+//
+// Sequences of a few thousand tokens give a warp of the kernel above one
+// short row: a chunk search, a ring fill and a few segments, a few round
+// trips for a few KB (64 sequences of 1024 tokens ran at half the copy
+// rate).  Here a block takes ROWS channel rows of one chunk and each warp
+// streams its ROWS / kCfaWarps rows (warp w: rows w, w + 8, ...) through
+// one ring that runs on from one row into the next, so the ring stays full
+// for the whole block.  The rows' weights, bias, prior and the x entries of
+// their new state are staged in shared memory once, while the ring fills.
+// Steps have the same arithmetic and edge handling as the kernel above; slot
+// indices and row positions are counters rather than constants.
+
+constexpr int kCfrRows = 64;        // channel rows per block
+constexpr int kCfrRowsMid = 128;    // for sequences of about a thousand tokens
+constexpr int kCfrRowsShort = 256;  // for sequences of a few hundred tokens
+// Segments start on a 32-byte boundary (whole sectors), not 256 bytes as in
+// the kernel above: a short row then wastes at most 15 tokens in front, and
+// a sequence's first chunk starts at its first token, its prior coming from
+// the window before segment 0 (1024-token sequences take 4 segments, not 5).
+constexpr int kCfrAlign = 16;
+static_assert(kCfaSlots == 8, "ring slot counters wrap with a mask");
+
+template <int W, bool SILU, int CHUNK, int ROWS>
+__global__ void __launch_bounds__(kCfaThreads, 4) fwd_cf_rows_kernel(const FwdArgs a) {
+    constexpr int kRowsPerWarp = ROWS / kCfaWarps;
+    extern __shared__ __align__(16) uint4 s_ring[];  // [kCfaSlots][kCfaThreads]
+    __shared__ uint16_t s_w[ROWS * W];               // [row][tap]
+    __shared__ uint16_t s_b[ROWS];
+    __shared__ uint32_t s_p[ROWS * 2];               // prior columns 0..3, packed
+    __shared__ uint16_t s_n[ROWS * 4];               // x entries of the new state
+    wait_prior_grid();  // no early release: see the note on the streaming kernels' launches
+    validate_sequence(a);
+    SeqChunk sc;  // block-uniform: every warp finds the same chunk
+    if (!locate_seq<kCfaPer>(a, CHUNK, blockIdx.x, sc)) return;
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int cbase = blockIdx.y * ROWS;
+    const int cbeg = sc.start + sc.chunk * CHUNK;
+    const int cend = sc.start + min(sc.len, (sc.chunk + 1) * CHUNK);
+    const bool chunk0 = sc.chunk == 0;
+    const bool keep = chunk0 && a.st != nullptr;
+    // first token read: a first chunk takes its prior from the state, a
+    // later chunk its W-1 halo tokens from x
+    const int need0 = chunk0 ? cbeg : cbeg - (W - 1);
+    // this warp's rows: cbase + warp + kCfaWarps * r, r < nr
+    const int nr = max(0, min(kRowsPerWarp, (a.dim - cbase - warp + kCfaWarps - 1) / kCfaWarps));
+    uint4 *const ring_base = s_ring + tid;
+
+    // Row r's input row, first aligned token and segment count.
+    auto geom = [&](int r, const uint16_t *&xc, int &a0, int &nseg) {
+        const int c = cbase + warp + kCfaWarps * r;
+        xc = a.x + c * a.xs_d;
+        const int phase = static_cast<int>((reinterpret_cast<uintptr_t>(xc) >> 1) & (kCfrAlign - 1));
+        a0 = need0 - ((phase + need0) & (kCfrAlign - 1));
+        nseg = (cend - a0 + 255) / 256;
+    };
+    // Issue side: the next (row, segment) to stream in and its slot.
+    int ir = 0, ij = 0, islot = 0, i_a0 = 0, i_nseg = 0;
+    const uint16_t *i_xc = a.x;
+    if (nr > 0) geom(0, i_xc, i_a0, i_nseg);
+    auto issue_next = [&]() {
+        if (ir < nr) {
+            const int t0 = i_a0 + ij * 256 + lane * 8;
+            uint4 *slot = ring_base + islot * kCfaThreads;
+            if (t0 >= 0 && t0 + 8 <= a.total) cp_async16(slot, i_xc + t0);
+            else *slot = cfa_ragged_vector(i_xc, t0, a.total);
+            if (++ij == i_nseg) {
+                ij = 0;
+                if (++ir < nr) geom(ir, i_xc, i_a0, i_nseg);
+            }
+        }
+        islot = (islot + 1) & (kCfaSlots - 1);
+        cp_async_commit();
+    };
+#pragma unroll
+    for (int j = 0; j < kCfaSlots - 1; ++j) issue_next();
+
+    // Stage the block's row parameters: thread = (row, part tid % 4).
+    for (int k = tid >> 2; k < ROWS; k += kCfaThreads / 4) {
+        const int part = tid & 3;
+        const int c = cbase + k;
+        if (c < a.dim) {
+            if (part == 0) {
+#pragma unroll
+                for (int t = 0; t < W; ++t) s_w[k * W + t] = __ldg(a.w + c * a.ws_d + t * a.ws_k);
+            } else if (part == 1) {
+                s_b[k] = a.bias ? __ldg(a.bias + c) : uint16_t(0);
+            } else if (part == 2) {
+                uint32_t p[4] = {0, 0, 0, 0};
+                if (keep && sc.init) {
+                    const uint16_t *sp = a.st + sc.line * a.ss_l + c * a.ss_d;
+#pragma unroll
+                    for (int j = 0; j < W - 1; ++j) p[j] = sp[j * a.ss_t];
+                }
+                s_p[2 * k] = p[0] | (p[1] << 16);
+                s_p[2 * k + 1] = p[2] | (p[3] << 16);
+            } else if (keep) {
+                const uint16_t *xr = a.x + c * a.xs_d;
+#pragma unroll
+                for (int j = 0; j < W - 1; ++j) {
+                    const int idx = sc.len + j;
+                    s_n[4 * k + j] = idx >= W - 1 ? xr[sc.start + idx - (W - 1)] : uint16_t(0);
+                }
+            }
+        }
+    }
+    __syncthreads();
+
+    uint32_t wt[W];
+    float bs = 0.0f;
+    uint32_t prior01 = 0, prior23 = 0;
+    uint32_t prev_z = 0, prev_w = 0;
+    auto window = [&](const uint4 &v, uint32_t (&E)[6]) {
+        const uint32_t up_z = __shfl_up_sync(kFullMask, v.z, 1);
+        const uint32_t up_w = __shfl_up_sync(kFullMask, v.w, 1);
+        const uint32_t pv_z = __shfl_sync(kFullMask, prev_z, 31);
+        const uint32_t pv_w = __shfl_sync(kFullMask, prev_w, 31);
+        prev_z = v.z;
+        prev_w = v.w;
+        E[0] = lane ? up_z : pv_z;
+        E[1] = lane ? up_w : pv_w;
+        E[2] = v.x;
+        E[3] = v.y;
+        E[4] = v.z;
+        E[5] = v.w;
+    };
+
+    int cr = 0, cj = 0, cslot = 0, c_a0 = 0, c_nseg = 0;
+    const uint16_t *c_xc = a.x;
+    uint16_t *oc = a.out;
+    while (cr < nr) {
+        cp_async_wait<kCfaSlots - 2>();
+        uint4 v = ring_base[cslot * kCfaThreads];
+        cslot = (cslot + 1) & (kCfaSlots - 1);
+        issue_next();
+        const int k = warp + kCfaWarps * cr;
+        if (cj == 0) {  // a new row: its geometry and parameters
+            geom(cr, c_xc, c_a0, c_nseg);
+            oc = a.out + (cbase + k) * a.os_d;
+#pragma unroll
+            for (int t = 0; t < W; ++t) wt[t] = 0x10001u * s_w[k * W + t];
+            bs = bf16_bits(s_b[k]);
+            prior01 = s_p[2 * k];
+            prior23 = s_p[2 * k + 1];
+            // the 4 tokens before segment 0: x before a later chunk's halo
+            // (never needed), the prior's last columns before a first chunk
+            prev_z = prev_w = 0;
+            if (chunk0) {
+                const uint4 before = cfa_with_prior<W>(make_uint4(0u, 0u, 0u, 0u), c_a0 - 8, cbeg,
+                                                       prior01, prior23);
+                prev_z = before.z;
+                prev_w = before.w;
+            }
+        }
+        const int t0 = c_a0 + cj * 256 + lane * 8;
+        if (cj == 0 && chunk0) v = cfa_with_prior<W>(v, t0, cbeg, prior01, prior23);
+        uint32_t E[6];
+        window(v, E);
+        if (t0 + 8 > cbeg && t0 < cend) {
+            const uint4 o = cfa_outputs<W, SILU>(E, wt, bs);
+            if (t0 >= cbeg && t0 + 8 <= cend) {
+                cfa_store(oc + t0, o);
+            } else {
+                const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int t = t0 + i;
+                    if (t >= cbeg && t < cend)
+                        oc[t] = uint16_t((i & 1) ? (ow[i >> 1] >> 16) : (ow[i >> 1] & 0xffffu));
+                }
+            }
+        }
+        if (++cj == c_nseg) {
+            if (keep && lane < W - 1) {
+                // New state = last W-1 entries of prior ++ x[sequence]; the
+                // block read every prior before its barrier.
+                const int idx = sc.len + lane;
+                uint16_t nb = s_n[4 * k + lane];
+                if (idx < W - 1) {
+                    const uint32_t src = idx < 2 ? prior01 : prior23;
+                    nb = uint16_t((idx & 1) ? (src >> 16) : (src & 0xffffu));
+                }
+                a.st[sc.line * a.ss_l + (cbase + k) * a.ss_d + lane * a.ss_t] = nb;
+            }
+            cj = 0;
+            ++cr;
+        }
+    }
+}
+
 // ------------------------------------------------------ short problems ----
 //
 // A problem too small to fill the machine with streaming chunks is set by
@@ -1367,6 +1559,24 @@ bool cf_long_chunks(int total, int batch) {
     return (static_cast<int64_t>(total) + batch - 1) / batch <= kCfaOneChunk;
 }
 
+
+// Sequences of at most kCfrMaxAvg tokens on average go to the multi-row
+// kernel, in chunks of kCfrChunk tokens, with more rows per block the
+// shorter they are: a block's fixed cost (chunk search, ring fill, staging)
+// then spreads over more data.  Measured at dim 8192, width 4 (us per call,
+// 64 / 128 / 256 rows per block): 16 x 2048 tokens 172 / 178 / 210, 64 x 1024
+// 369 / 359 / 373, 128 x 512 463 / 441 / 436, 256 x 256 665 / 613 / 593; the
+// single-row kernel took 206, 607, 999 and 1870.  At 16 x 3072 the two
+// kernels tie (248 and 251 us); at 16 x 4096 the single-row one wins (305
+// against 334).
+constexpr int kCfrMaxAvg = 3072;
+constexpr int kCfrMidAvg = 1024;
+constexpr int kCfrShortAvg = 512;
+constexpr int kCfrChunk = kCfaChunkSplit;
+
+int64_t average_length(int total, int batch) { return (static_cast<int64_t>(total) + batch - 1) / batch; }
+bool cf_short_rows(int total, int batch) { return average_length(total, batch) <= kCfrMaxAvg; }
+
 template <int W, bool SILU>
 int launch_cl_async_w(const FwdArgs &a, cudaStream_t stream) {
     int dev = 0;
@@ -1394,8 +1604,27 @@ int launch_cf_async_chunk(const FwdArgs &a, cudaStream_t stream) {
     return launch_pdl(fwd_cf_async_kernel<W, SILU, CHUNK>, grid, dim3(kCfaThreads), kCfaSmem, stream, a);
 }
 
+template <int W, bool SILU, int CHUNK, int ROWS>
+int launch_cf_rows_chunk(const FwdArgs &a, cudaStream_t stream) {
+    int dev = 0;
+    current_device_sms(&dev);
+    cudaError_t e;
+    if (resident_blocks<fwd_cf_rows_kernel<W, SILU, CHUNK, ROWS>>(kCfaThreads, kCfaSmem, dev, &e) == 0)
+        return static_cast<int>(e);
+    const dim3 grid(static_cast<unsigned>(a.total / CHUNK + a.batch),
+                    static_cast<unsigned>((a.dim + ROWS - 1) / ROWS));
+    return launch_pdl(fwd_cf_rows_kernel<W, SILU, CHUNK, ROWS>, grid, dim3(kCfaThreads), kCfaSmem, stream,
+                      a);
+}
+
 template <int W, bool SILU>
 int launch_cf_async_w(const FwdArgs &a, cudaStream_t stream) {
+    if (cf_short_rows(a.total, a.batch)) {
+        const int64_t avg = average_length(a.total, a.batch);
+        if (avg <= kCfrShortAvg) return launch_cf_rows_chunk<W, SILU, kCfrChunk, kCfrRowsShort>(a, stream);
+        if (avg <= kCfrMidAvg) return launch_cf_rows_chunk<W, SILU, kCfrChunk, kCfrRowsMid>(a, stream);
+        return launch_cf_rows_chunk<W, SILU, kCfrChunk, kCfrRows>(a, stream);
+    }
     return cf_long_chunks(a.total, a.batch) ? launch_cf_async_chunk<W, SILU, kCfaChunk>(a, stream)
                                             : launch_cf_async_chunk<W, SILU, kCfaChunkSplit>(a, stream);
 }

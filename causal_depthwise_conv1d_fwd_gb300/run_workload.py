@@ -10,7 +10,8 @@ spec (speculative verify, 64 rows x 4 drafts, dim 8192), atrex (one
 channel-first sequence of --tokens x --dim, the atrex-bench #003 shapes),
 paged_streams (a layer's four conv streams on one paged cache, one launch),
 varlen (8 sequences of 1..512 tokens, dim 4096, channel-last), paged_single
-(the paged workload as one paged_sconv_fwd_with_metadata launch).
+(the paged workload as one paged_sconv_fwd_with_metadata launch), many (--batch
+channel-first sequences of --tokens tokens each at --dim, all with initial state).
 The process exits 0 after a device synchronize; it times nothing.
 """
 from __future__ import annotations
@@ -23,14 +24,14 @@ from . import api
 from . import workloads as wl
 
 PARTS = ("prefill_tokens_dim", "prefill_dim_tokens", "decode", "paged", "spec", "atrex",
-         "paged_streams", "varlen", "paged_single")
+         "paged_streams", "varlen", "paged_single", "many")
 
 
 def _dev(kwargs, dev):
     return {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in kwargs.items()}
 
 
-def make_launch(part: str, dev, tokens: int = 1024, dim: int = 4096, width: int = 4):
+def make_launch(part: str, dev, tokens: int = 1024, dim: int = 4096, width: int = 4, batch: int = 64):
     if part.startswith("prefill"):
         layout = "tokens_dim" if part.endswith("tokens_dim") else "dim_tokens"
         c = wl.config_large_prefill(layout=layout)
@@ -87,6 +88,14 @@ def make_launch(part: str, dev, tokens: int = 1024, dim: int = 4096, width: int 
                                   device=dev)
         launch = api.prepare_ccv_fwd(**d, out=out)
         return lambda: launch()
+    if part == "many":
+        c = wl.varlen_prefill(1010, [tokens] * batch, dim, width, layout="dim_tokens",
+                              has_init="all")
+        d = _dev(c.kwargs(), dev)
+        out = torch.empty_strided(d["x"].shape, d["x"].stride(), dtype=torch.bfloat16,
+                                  device=dev)
+        launch = api.prepare_ccv_fwd(**d, out=out)
+        return lambda: launch()
     if part == "varlen":
         d = _dev(wl.config_varlen().kwargs(), dev)
         out = torch.empty_strided(d["x"].shape, d["x"].stride(), dtype=torch.bfloat16,
@@ -110,13 +119,14 @@ def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--part", choices=PARTS, required=True)
     ap.add_argument("--reps", type=int, default=3)
-    ap.add_argument("--tokens", type=int, default=1024, help="atrex part only")
-    ap.add_argument("--dim", type=int, default=4096, help="atrex part only")
+    ap.add_argument("--tokens", type=int, default=1024, help="atrex and many parts only")
+    ap.add_argument("--dim", type=int, default=4096, help="atrex and many parts only")
+    ap.add_argument("--batch", type=int, default=64, help="many part only")
     ap.add_argument("--width", type=int, default=4, help="prefill parts only: conv width 2..5")
     args = ap.parse_args(argv)
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    run = make_launch(args.part, dev, args.tokens, args.dim, args.width)
+    run = make_launch(args.part, dev, args.tokens, args.dim, args.width, args.batch)
     for _ in range(args.reps):
         run()
     torch.cuda.synchronize()

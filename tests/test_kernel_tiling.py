@@ -20,6 +20,12 @@ checks that:
 - the segments cover the chunk and fit the chunk's segment budget;
 - every segment starts on the 256-byte boundary the alignment promises.
 
+Multi-row channel-first kernel: fwd_cf_rows_kernel runs one ring across a
+warp's rows, with counters for the issue and consume positions; a replay of
+those counters checks the ring's order, slots and commit groups and that
+each row's outputs are stored once.  The channel-first streaming kernels
+search with four candidates per lane in the final round.
+
 Short problems: fwd_cl_short_kernel and fwd_cf_short_kernel find their chunk
 with a search whose final round also fetches every candidate's end, state
 line and flag; a replay checks that every chunk gets exactly one slot.  The
@@ -44,8 +50,9 @@ def _constants():
     src = open(os.path.join(CSRC, "ccv_fwd.cu")).read()
     common = open(os.path.join(CSRC, "ccv_common.cuh")).read()
     env = {"kMaxWidth": int(re.search(r"constexpr int kMaxWidth = (\d+);", common).group(1))}
-    for name in ("kCfaSegs", "kCfaAlign", "kCfaSlots", "kCfaChunk", "kCaThreads", "kCaWarps",
-                 "kCaRun", "kCaChunk", "kShortRun", "kShortSegs", "kShortCfChunk"):
+    for name in ("kCfaSegs", "kCfaAlign", "kCfaSlots", "kCfaChunk", "kCfaChunkSplit", "kCfaPer",
+                 "kCfrChunk", "kCfrRows", "kCfrRowsMid", "kCfrRowsShort", "kCfrAlign", "kCaThreads", "kCaWarps", "kCaRun", "kCaChunk",
+                 "kShortRun", "kShortSegs", "kShortCfChunk"):
         expr = re.search(rf"constexpr int {name} = ([^;]+);", src).group(1)
         env[name] = int(eval(expr, {"__builtins__": {}}, dict(env)))
     return env
@@ -183,7 +190,7 @@ def locate(qsl, total, C, slot):
     return lo, k
 
 
-@pytest.mark.parametrize("C", ["kCaChunk", "kCfaChunk"])
+@pytest.mark.parametrize("C", ["kCaChunk"])
 def test_chunk_slots_cover_every_chunk_once(C):
     import random
 
@@ -207,12 +214,14 @@ def test_chunk_slots_cover_every_chunk_once(C):
         assert set(found) == want
 
 
-def locate_short(qsl, total, C, slot):
-    """The short kernels' search: 32-wide narrowing rounds while more than 32
-    candidates remain, then one round over at most 32 candidates that picks
-    the last with floor(qsl[i] / C) + i <= slot."""
+def locate_short(qsl, total, C, slot, per=1):
+    """The one-round-trip search (locate_seq): 32-wide narrowing rounds while
+    more than 32 * per candidates remain, then one round in which lane l
+    takes candidates per*l .. per*l+per-1 and the last candidate with
+    floor(qsl[i] / C) + i <= slot of the highest such lane wins.  per = 1 in
+    the short kernels, kCfaPer in the channel-first streaming kernels."""
     lo, n = 0, len(qsl) - 1
-    while n > 32:
+    while n > 32 * per:
         stride = (n + 31) >> 5
         mask = 0
         for lane in range(32):
@@ -224,13 +233,18 @@ def locate_short(qsl, total, C, slot):
         top = mask.bit_length() - 1
         lo += top * stride
         n = min(stride, n - top * stride)
-    mask = 0
+    mask, pick = 0, [-1] * 32
     for lane in range(32):
-        if lane < n and qsl[lo + lane] // C + lo + lane <= slot:
+        for k in range(per):
+            i = per * lane + k
+            if i < n and qsl[lo + i] // C + lo + i <= slot:
+                pick[lane] = k
+        if pick[lane] >= 0:
             mask |= 1 << lane
     if mask == 0:
         return None
-    seq = lo + mask.bit_length() - 1
+    top = mask.bit_length() - 1
+    seq = lo + per * top + pick[top]
     start, end = qsl[seq], qsl[seq + 1]
     if start < 0 or end < start or end > total:
         return None
@@ -240,14 +254,16 @@ def locate_short(qsl, total, C, slot):
     return seq, k
 
 
-@pytest.mark.parametrize("C", ["kShortRun", "kShortCfChunk"])
-def test_short_chunk_slots_cover_every_chunk_once(C):
+@pytest.mark.parametrize("C, per", [("kShortRun", 1), ("kShortCfChunk", 1), ("kCfaChunk", "kCfaPer"),
+                                    ("kCfaChunkSplit", "kCfaPer"), ("kCfrChunk", "kCfaPer")])
+def test_short_chunk_slots_cover_every_chunk_once(C, per):
     import random
 
     C = K[C]
+    per = K[per] if isinstance(per, str) else per
     rng = random.Random(11)
     for trial in range(60):
-        batch = rng.choice([1, 2, 3, 31, 32, 33, 100, 1025])
+        batch = rng.choice([1, 2, 3, 31, 32, 33, 100, 127, 128, 129, 1025, 4200])
         lens = [rng.choice([0, 1, 2, C - 1, C, C + 1, rng.randrange(0, 3 * C)])
                 for _ in range(batch)]
         qsl = [0]
@@ -256,7 +272,7 @@ def test_short_chunk_slots_cover_every_chunk_once(C):
         total = qsl[-1] + rng.choice([0, 0, 5])
         found = {}
         for slot in range(total // C + batch):
-            r = locate_short(qsl, total, C, slot)
+            r = locate_short(qsl, total, C, slot, per)
             if r is not None:
                 assert r not in found, f"chunk {r} found by slots {found[r]} and {slot}"
                 found[r] = slot
@@ -298,3 +314,85 @@ def test_short_channel_first_window(W):
                             else:
                                 stored += [t for t in range(t0, t0 + 8) if cbeg <= t < cend]
                     assert sorted(stored) == list(range(cbeg, cend)), (total, start, chunk, phase)
+
+
+def replay_rows(phases, cbeg, cend, chunk0, W):
+    """Follow one warp of fwd_cf_rows_kernel: rows with the given phases (in
+    tokens mod kCfrAlign), one ring of kCfaSlots slots run across them with
+    an issue counter and a consume counter, as in the kernel."""
+    S, A = K["kCfaSlots"], K["kCfrAlign"]
+    need0 = cbeg if chunk0 else cbeg - (W - 1)
+    geo = []
+    for ph in phases:
+        a0 = need0 - ((ph + need0) & (A - 1))
+        geo.append((a0, (cend - a0 + SEG - 1) // SEG))
+    nr = len(phases)
+    issues, st = [], dict(ir=0, ij=0, islot=0, groups=0)
+
+    def issue_next(step):
+        if st["ir"] < nr:
+            issues.append((st["ir"], st["ij"], st["islot"], st["groups"], step))
+            st["ij"] += 1
+            if st["ij"] == geo[st["ir"]][1]:
+                st["ij"], st["ir"] = 0, st["ir"] + 1
+        st["islot"] = (st["islot"] + 1) & (S - 1)
+        st["groups"] += 1  # one commit group per call, empty or not
+
+    for _ in range(S - 1):
+        issue_next(-1)
+    cr = cj = cslot = step = 0
+    consumes, stored = [], {r: [] for r in range(nr)}
+    while cr < nr:
+        complete = st["groups"] - (S - 2)  # groups 0 .. complete-1 have landed
+        consumes.append((cr, cj, cslot, complete, step))
+        cslot = (cslot + 1) & (S - 1)
+        issue_next(step)
+        a0 = geo[cr][0]
+        for lane in range(32):
+            t0 = a0 + cj * SEG + lane * 8
+            stored[cr] += [t for t in range(t0, t0 + 8) if cbeg <= t < cend]
+        cj += 1
+        if cj == geo[cr][1]:
+            cj, cr = 0, cr + 1
+        step += 1
+    return geo, issues, consumes, stored
+
+
+@pytest.mark.parametrize("W", [2, 4, 5])
+def test_rows_kernel_ring_runs_across_rows(W):
+    """Every (row, segment) of a warp's rows is issued once and consumed once,
+    in the same order and through the same slot, after its commit group has
+    landed and before the slot is issued again; each row's segments start
+    on the aligned boundary at or before its first token read (a first
+    chunk's first token, a later chunk's first halo token), the inputs its
+    outputs need lie in the segments or, for a first chunk, in the 4 tokens
+    before them that the prior fills, and each output token is stored
+    exactly once."""
+    C, A, S = K["kCfrChunk"], K["kCfrAlign"], K["kCfaSlots"]
+    per_warp = max(K["kCfrRows"], K["kCfrRowsMid"], K["kCfrRowsShort"]) // 8
+    import random
+
+    rng = random.Random(23)
+    for trial in range(300):
+        start = rng.choice([0, 1, 7, 8, 100, 4099])
+        length = rng.choice([1, 2, 3, 5, 255, 256, 257, 1000, C - 1, C, C + 1, 2 * C + 3])
+        nr = rng.randint(1, per_warp)
+        stride = rng.choice([0, 1, 8, 13, 64])  # row-to-row phase step
+        phase0 = rng.randrange(A)
+        phases = [(phase0 + r * stride) % A for r in range(nr)]
+        for chunk in range((length + C - 1) // C):
+            cbeg = start + chunk * C
+            cend = start + min(length, (chunk + 1) * C)
+            chunk0 = chunk == 0
+            geo, issues, consumes, stored = replay_rows(phases, cbeg, cend, chunk0, W)
+            assert [i[:3] for i in issues] == [c[:3] for c in consumes]
+            for m, (iss, con) in enumerate(zip(issues, consumes)):
+                assert iss[3] < con[3], f"item {m} read before its group landed"
+                if m + S < len(issues):
+                    assert issues[m + S][4] >= con[4], f"slot of item {m} reissued before it was read"
+            for r, (a0, nseg) in enumerate(geo):
+                need0 = cbeg if chunk0 else cbeg - (W - 1)
+                assert (phases[r] + a0) % A == 0 and need0 - A < a0 <= need0
+                held_from = a0 - 4 if chunk0 else a0  # the prior fills a0-4 .. a0-1
+                assert held_from <= cbeg - (W - 1) and a0 + nseg * SEG >= cend
+                assert sorted(stored[r]) == list(range(cbeg, cend))

@@ -152,18 +152,30 @@ def test_channel_first_chunk_edges(width, extra):
     check(case)
 
 
+def _kernel_constant(name):
+    import re
+
+    src = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                            "causal_depthwise_conv1d_fwd_gb300", "csrc", "ccv_fwd.cu")).read()
+    return int(re.search(rf"constexpr int {name} = (\d+);", src).group(1))
+
+
 def _cf_chunk_tokens(total, batch):
-    """The host's choice of channel-first chunk length (cf_long_chunks in the
-    kernel source), with its constants read from the source."""
+    """The host's choice of channel-first streaming kernel and chunk length
+    (cf_short_rows and cf_long_chunks in the kernel source), with its
+    constants read from the source: the multi-row kernel's kCfrChunk up to
+    kCfrMaxAvg tokens per sequence on average, one kCfaChunk-token chunk per
+    sequence up to kCfaOneChunk, kCfaChunkSplit-token chunks above."""
     import re
 
     src = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
                             "causal_depthwise_conv1d_fwd_gb300", "csrc", "ccv_fwd.cu")).read()
     one = int(re.search(r"constexpr int kCfaOneChunk = (\d+);", src).group(1))
-    split_expr = re.search(r"constexpr int kCfaChunkSplit = ([^;]+);", src).group(1)
-    split = int(eval(split_expr, {"__builtins__": {}}, {"kCfaAlign": TILING["kCfaAlign"]}))
+    rows_max = int(re.search(r"constexpr int kCfrMaxAvg = (\d+);", src).group(1))
     avg = -(-total // batch)
-    return TILING["kCfaChunk"] if avg <= one else split
+    if avg <= rows_max:
+        return TILING["kCfrChunk"]
+    return TILING["kCfaChunk"] if avg <= one else TILING["kCfaChunkSplit"]
 
 
 def _lengths_around_cf_chunk():
@@ -175,12 +187,47 @@ def _lengths_around_cf_chunk():
     return head + [70000]
 
 
+def _lengths_around_rows_chunk(max_avg=None):
+    """Sequence lengths c-1, c, c+1, 2c+1 and 3 around the multi-row
+    kernel's chunk length c, then short fillers (1 to 60 tokens) until the
+    average is at most max_avg (default: the multi-row kernel's limit)."""
+    c = TILING["kCfrChunk"]
+    max_avg = max_avg or _kernel_constant("kCfrMaxAvg")
+    lengths = [c - 1, c, c + 1, 2 * c + 1, 3]
+    fill = [1, 2, 3, 5, 60, 17]
+    while -(-sum(lengths) // len(lengths)) > max_avg:
+        lengths.append(fill[len(lengths) % len(fill)])
+    return lengths
+
+
 def test_chunk_edge_lengths_sit_on_the_chosen_chunk():
-    """The chunk-edge cases above straddle the chunk length the host picks."""
+    """The chunk-edge cases straddle the chunk length the host picks: the
+    split chunk of long sequences, and the multi-row kernel's chunk."""
     lengths = _lengths_around_cf_chunk()
     c = lengths[1]
     assert _cf_chunk_tokens(sum(lengths), len(lengths)) == c
-    assert c < TILING["kCfaChunk"]  # the split chunk, not one chunk per sequence
+    assert c == TILING["kCfaChunkSplit"] < TILING["kCfaChunk"]
+    lengths = _lengths_around_rows_chunk()
+    assert _cf_chunk_tokens(sum(lengths), len(lengths)) == lengths[1] == TILING["kCfrChunk"]
+
+
+@pytest.mark.parametrize("width", [2, 4, 5])
+@pytest.mark.parametrize("dim, extra", [(8, 0), (72, 3), (300, 1)])
+@pytest.mark.parametrize("limit, above", [("kCfrMaxAvg", "kCfrMidAvg"), ("kCfrMidAvg", "kCfrShortAvg"),
+                                          ("kCfrShortAvg", None)])
+def test_channel_first_rows_chunk_edges(width, dim, extra, limit, above):
+    """The multi-row kernel (blocks of 64, 128 or 256 channel rows by the
+    average sequence length; one ring running across each warp's rows) on
+    sequences one token short of, at and past its chunk length and of two
+    chunks among short fillers; dims of one partial row group, of full
+    groups plus a partial one, and rows at several 16-byte phases."""
+    lengths = _lengths_around_rows_chunk(_kernel_constant(limit))
+    if above is not None:  # the average picks this block size, not the next
+        assert -(-sum(lengths) // len(lengths)) > _kernel_constant(above)
+    case = wl.varlen_prefill(560 + width + dim + extra, lengths, dim, width,
+                             num_cache_lines=len(lengths) + 2, layout="dim_tokens",
+                             has_init="bernoulli", extra_tokens=extra)
+    check(case)
 
 
 @pytest.mark.parametrize("extra", [0, 1, 3, 5])
@@ -429,8 +476,9 @@ def test_automatic_choice_at_its_threshold(prefill_path, monkeypatch, layout, to
     d = to_device(case.kwargs(), DEV)
     names = _kernel_names(lambda: ccv.ccv_fwd(**d))
     if names is not None:
-        want = "short" if tokens * 4096 <= (1 << 23) else "async"
-        assert any(want in n for n in names), names
+        # streaming: fwd_cl_async, fwd_cf_async or, for short sequences, fwd_cf_rows
+        want = ("short",) if tokens * 4096 <= (1 << 23) else ("async", "rows")
+        assert any(w in n for n in names for w in want), names
 
 
 @pytest.mark.parametrize("layout", ["tokens_dim", "dim_tokens"])
