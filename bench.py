@@ -521,22 +521,28 @@ def run_e2e(dev, cases, dev_args, steps):
 
     for st in all_streams:
         st.wait_stream(stream)
-    one_step()
-    join()
-    torch.cuda.synchronize()
-    barrier(dev)
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    for st in all_streams:
-        st.wait_stream(stream)
-    for _ in range(steps):
+    for _ in range(3):
         one_step()
     join()
-    end.record(stream)
     torch.cuda.synchronize()
-    barrier(dev)
-    return start.elapsed_time(end) / 1e3, h2d, d2h
+    # Three timed windows of `steps` steps each; the median window is the
+    # result (single windows varied by up to 12% from run to run).
+    windows = []
+    for _ in range(3):
+        barrier(dev)
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for st in all_streams:
+            st.wait_stream(stream)
+        for _ in range(steps):
+            one_step()
+        join()
+        end.record(stream)
+        torch.cuda.synchronize()
+        barrier(dev)
+        windows.append(start.elapsed_time(end) / 1e3)
+    return sorted(windows)[1], h2d, d2h, windows
 
 
 GRAPH_CALLS = 20  # calls captured per graph, so replay measures the GPU, not the host launch
@@ -1067,6 +1073,35 @@ def copy_same_size_timing(x, calls=50):
             "gbs_event_bracketed": round(nbytes / (single * 1e-6) / 1e9, 1)}
 
 
+def marginal_timing(parts, steps, stream):
+    """What each part adds to the headline loop: the loop of K steps with every
+    part, and with each part left out in turn (the rest in step order, nothing
+    between the launches), timed with events around each loop.  A part's
+    marginal time is the step's time minus the time without it, so it counts
+    only what does not overlap its neighbours' launches and tails."""
+    def loop_us(keep):
+        for _ in range(5):
+            for p in keep:
+                p.fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(steps):
+            for p in keep:
+                p.fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e3 / steps
+
+    full = loop_us(parts)
+    out = {}
+    for p in parts:
+        out[p.name] = round(full - loop_us([q for q in parts if q is not p]), 2)
+    full_again = loop_us(parts)
+    return {"step_us": round((full + full_again) / 2, 2), "marginal_us": out,
+            "steps": steps}
+
+
 def concurrent_streams_timing(parts, steps):
     """The step's parts on two streams at once: the prefill parts on one,
     decode and paged on another (they share no buffer), as an engine would
@@ -1150,6 +1185,7 @@ def run_ours(args):
     graph = graph_step_timing(parts, args.steps)
     b2b = {p.name: back_to_back_us(p) for p in parts if p.name.startswith("prefill")}
     concurrent = concurrent_streams_timing(parts, args.steps)
+    marginal = marginal_timing(parts, min(args.steps, 2000), stream)
 
     step_bytes = sum(p.nbytes for p in parts)
     value = whole_job_rate(step_bytes, args.steps, world, max_seconds) / 1e9
@@ -1164,7 +1200,7 @@ def run_ours(args):
     traffic = recorded_traffic(dominant.kernel)
 
     e2e_steps = max(3, min(args.steps, args.e2e_steps))
-    e2e_s, h2d, d2h = run_e2e(dev, cases, dev_args, e2e_steps)
+    e2e_s, h2d, d2h, e2e_windows = run_e2e(dev, cases, dev_args, e2e_steps)
     e2e_s = max_over_ranks(e2e_s, dev)
     e2e_value = whole_job_rate(step_bytes, e2e_steps, world, e2e_s) / 1e9
     link = host_link_peak(dev)
@@ -1240,6 +1276,7 @@ def run_ours(args):
         "paged_single_launch": paged_single,
         "width_variants": widths,
         "short_sequences": short_seqs,
+        "marginal_in_step": marginal,
         "small_configs": small,
         "launch_floor_us": floor,
         "copy_same_size": copy_ref,
@@ -1250,6 +1287,8 @@ def run_ours(args):
                      "algorithmic_bytes_per_launch": dominant.nbytes // dominant.launches,
                      "avg_launch_us": round(dom_us, 2)},
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "steps": e2e_steps,
+                "windows": 3, "window_gbs": [round(step_bytes * e2e_steps / w / 1e9, 1)
+                                              for w in e2e_windows],
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "link_gbs": round(link_gbs, 1), "link_peak_gbs": link["both_gbs"],
                 "frac_of_link": round(link_gbs / link["both_gbs"], 4), "link_peak": link},

@@ -1089,9 +1089,10 @@ template <int W, bool SILU, int CHUNK, int ROWS>
 __global__ void __launch_bounds__(kCfaThreads, 4) fwd_cf_rows_kernel(const FwdArgs a) {
     constexpr int kRowsPerWarp = ROWS / kCfaWarps;
     extern __shared__ __align__(16) uint4 s_ring[];  // [kCfaSlots][kCfaThreads]
-    __shared__ uint16_t s_w[ROWS * W];               // [row][tap]
-    __shared__ uint16_t s_b[ROWS];
+    __shared__ uint32_t s_w[ROWS * W];               // [row][tap], bf16 weight in both halves
+    __shared__ float s_b[ROWS];
     __shared__ uint32_t s_p[ROWS * 2];               // prior columns 0..3, packed
+    __shared__ uint32_t s_pre[ROWS * 2];             // the 4 tokens before segment 0, packed
     __shared__ uint16_t s_n[ROWS * 4];               // x entries of the new state
     wait_prior_grid();  // no early release: see the note on the streaming kernels' launches
     validate_sequence(a);
@@ -1112,13 +1113,16 @@ __global__ void __launch_bounds__(kCfaThreads, 4) fwd_cf_rows_kernel(const FwdAr
     const int nr = max(0, min(kRowsPerWarp, (a.dim - cbase - warp + kCfaWarps - 1) / kCfaWarps));
     uint4 *const ring_base = s_ring + tid;
 
-    // Row r's input row, first aligned token and segment count.
-    auto geom = [&](int r, const uint16_t *&xc, int &a0, int &nseg) {
-        const int c = cbase + warp + kCfaWarps * r;
+    // Channel row c's input row, first aligned token and segment count.
+    auto geom_of = [&](int c, const uint16_t *&xc, int &a0, int &nseg) {
         xc = a.x + c * a.xs_d;
         const int phase = static_cast<int>((reinterpret_cast<uintptr_t>(xc) >> 1) & (kCfrAlign - 1));
         a0 = need0 - ((phase + need0) & (kCfrAlign - 1));
         nseg = (cend - a0 + 255) / 256;
+    };
+    // The same for this warp's row r.
+    auto geom = [&](int r, const uint16_t *&xc, int &a0, int &nseg) {
+        geom_of(cbase + warp + kCfaWarps * r, xc, a0, nseg);
     };
     // Issue side: the next (row, segment) to stream in and its slot.
     int ir = 0, ij = 0, islot = 0, i_a0 = 0, i_nseg = 0;
@@ -1148,9 +1152,9 @@ __global__ void __launch_bounds__(kCfaThreads, 4) fwd_cf_rows_kernel(const FwdAr
         if (c < a.dim) {
             if (part == 0) {
 #pragma unroll
-                for (int t = 0; t < W; ++t) s_w[k * W + t] = __ldg(a.w + c * a.ws_d + t * a.ws_k);
+                for (int t = 0; t < W; ++t) s_w[k * W + t] = 0x10001u * __ldg(a.w + c * a.ws_d + t * a.ws_k);
             } else if (part == 1) {
-                s_b[k] = a.bias ? __ldg(a.bias + c) : uint16_t(0);
+                s_b[k] = a.bias ? bf16_bits(__ldg(a.bias + c)) : 0.0f;
             } else if (part == 2) {
                 uint32_t p[4] = {0, 0, 0, 0};
                 if (keep && sc.init) {
@@ -1158,8 +1162,21 @@ __global__ void __launch_bounds__(kCfaThreads, 4) fwd_cf_rows_kernel(const FwdAr
 #pragma unroll
                     for (int j = 0; j < W - 1; ++j) p[j] = sp[j * a.ss_t];
                 }
-                s_p[2 * k] = p[0] | (p[1] << 16);
-                s_p[2 * k + 1] = p[2] | (p[3] << 16);
+                const uint32_t p01 = p[0] | (p[1] << 16), p23 = p[2] | (p[3] << 16);
+                s_p[2 * k] = p01;
+                s_p[2 * k + 1] = p23;
+                // The 4 tokens before segment 0: x before a later chunk's
+                // halo (never needed), the prior's last columns before a
+                // first chunk.
+                uint4 before = make_uint4(0u, 0u, 0u, 0u);
+                if (chunk0) {
+                    const uint16_t *xr;
+                    int a0, nseg;
+                    geom_of(c, xr, a0, nseg);
+                    before = cfa_with_prior<W>(before, a0 - 8, cbeg, p01, p23);
+                }
+                s_pre[2 * k] = before.z;
+                s_pre[2 * k + 1] = before.w;
             } else if (keep) {
                 const uint16_t *xr = a.x + c * a.xs_d;
 #pragma unroll
@@ -1204,19 +1221,12 @@ __global__ void __launch_bounds__(kCfaThreads, 4) fwd_cf_rows_kernel(const FwdAr
             geom(cr, c_xc, c_a0, c_nseg);
             oc = a.out + (cbase + k) * a.os_d;
 #pragma unroll
-            for (int t = 0; t < W; ++t) wt[t] = 0x10001u * s_w[k * W + t];
-            bs = bf16_bits(s_b[k]);
+            for (int t = 0; t < W; ++t) wt[t] = s_w[k * W + t];
+            bs = s_b[k];
             prior01 = s_p[2 * k];
             prior23 = s_p[2 * k + 1];
-            // the 4 tokens before segment 0: x before a later chunk's halo
-            // (never needed), the prior's last columns before a first chunk
-            prev_z = prev_w = 0;
-            if (chunk0) {
-                const uint4 before = cfa_with_prior<W>(make_uint4(0u, 0u, 0u, 0u), c_a0 - 8, cbeg,
-                                                       prior01, prior23);
-                prev_z = before.z;
-                prev_w = before.w;
-            }
+            prev_z = s_pre[2 * k];
+            prev_w = s_pre[2 * k + 1];
         }
         const int t0 = c_a0 + cj * 256 + lane * 8;
         if (cj == 0 && chunk0) v = cfa_with_prior<W>(v, t0, cbeg, prior01, prior23);
