@@ -287,6 +287,7 @@ KERNEL_SOURCE = {
     "fwd_cf_async_kernel": "ccv_fwd.cu",
     "fwd_cl_short_kernel": "ccv_fwd.cu",
     "fwd_cf_short_kernel": "ccv_fwd.cu",
+    "fwd_cf_rows_kernel": "ccv_fwd.cu",
     "update_kernel": "ccv_update.cu",
     "spec_kernel": "ccv_update.cu",
     "paged_row_kernel": "paged_sconv.cu",
