@@ -96,7 +96,12 @@ int ccv_version(void);
  * Two non-pad sequences that share a state line race (undefined result).
  * Problems of up to 2^23 elements (total_tokens * dim) run on kernels built
  * for latency, larger ones on streaming kernels; both compute the same
- * results.  The environment variable CCV_PREFILL_PATH=short or =stream,
+ * results.  In the channel-first layout the streaming family has a kernel
+ * for sequences of a few thousand tokens or fewer on average (several
+ * channel rows per warp) and one for longer ones.  Every choice and every
+ * grid follows from the sizes (total_tokens, batch, dim, width), the strides
+ * and the buffers' alignment, never from query_start_loc, so a captured
+ * graph stays valid for any offsets of the same sizes.  The environment variable CCV_PREFILL_PATH=short or =stream,
  * read at each call, forces one family (for testing and tuning).
  */
 int ccv_fwd(const void *x, int64_t x_stride_dim, int64_t x_stride_tok,
