@@ -481,6 +481,33 @@ def test_automatic_choice_at_its_threshold(prefill_path, monkeypatch, layout, to
         assert any(w in n for n in names for w in want), names
 
 
+@pytest.mark.parametrize("avg, want, rows", [(512, "fwd_cf_rows_kernel", 256),
+                                             (1024, "fwd_cf_rows_kernel", 128),
+                                             (3072, "fwd_cf_rows_kernel", 64),
+                                             (3073, "fwd_cf_async_kernel", None)])
+def test_channel_first_streaming_choice(prefill_path, avg, want, rows):
+    """The host picks the channel-first streaming kernel from the average
+    sequence length: the multi-row kernel up to kCfrMaxAvg tokens (256, 128
+    or 64 rows per block by kCfrShortAvg and kCfrMidAvg), the single-row one
+    above.  Lengths with that average at dim 1024, streaming kernels forced,
+    match the oracle and launch the expected kernel."""
+    if prefill_path == "short":
+        pytest.skip("the streaming choice only")
+    assert _kernel_constant("kCfrMaxAvg") == 3072 and _kernel_constant("kCfrMidAvg") == 1024
+    assert _kernel_constant("kCfrShortAvg") == 512
+    batch = 4
+    lengths = [avg - 7, avg + 3, avg + 7, avg - 3]  # mean avg; ceil(total / batch) == avg
+    case = wl.varlen_prefill(1900 + avg, lengths, 1024, 4, num_cache_lines=batch,
+                             layout="dim_tokens", has_init="bernoulli")
+    check(case)
+    d = to_device(case.kwargs(), DEV)
+    names = _kernel_names(lambda: ccv.ccv_fwd(**d))
+    if names is not None:
+        assert any(want in n for n in names), names
+        if rows is not None:
+            assert any(f", {rows}>" in n for n in names), names
+
+
 @pytest.mark.parametrize("layout", ["tokens_dim", "dim_tokens"])
 @pytest.mark.parametrize("batch", [33, 100, 128, 129, 1100, 4200])
 def test_many_sequences(layout, batch):
